@@ -1,0 +1,210 @@
+// api.cu -- the C ABI of libkvq (declared in include/kvq.h): argument validation, sizing
+// helpers, and the launches.  Every check here runs on the host before any kernel is
+// enqueued, so a rejected call moves no byte; there is no CPU fallback for anything.
+#include <stdio.h>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* ring, const int32_t* start_pos,
+                  const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows, int lanes,
+                  const __nv_bfloat16* k, const __nv_bfloat16* v, cudaStream_t stream);
+struct AttnArgs;
+int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t stream);
+int launch_decode_hq2b(const AttnArgs& a, cudaStream_t stream);
+int decode_split_tokens(int fmt);
+int prefill_split_tokens(int fmt);
+}  // namespace kvq
+
+#include "attn_args.cuh"
+
+using namespace kvq;
+
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+
+int check_geom(const kvq_geom* g) {
+  if (!g) return KVQ_ERR_INVALID_ARG;
+  if (g->format != KVQ_FMT_HQ2B && g->format != KVQ_FMT_BF16) return KVQ_ERR_UNSUPPORTED;
+  if (g->head_dim != D || g->page_tokens != P) return KVQ_ERR_UNSUPPORTED;
+  if (g->num_layers <= 0 || g->num_kv_heads <= 0 || g->num_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  if (g->num_layers > 4096 || g->num_kv_heads > 1024) return KVQ_ERR_UNSUPPORTED;
+  if (g->num_q_heads % g->num_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (g->num_q_heads / g->num_kv_heads > MAX_GROUP) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t page_bytes_of(const kvq_geom* g) {
+  return (size_t)g->num_layers * g->num_kv_heads * 2 * (size_t)block_bytes(g->format);
+}
+
+size_t partial_bytes(int64_t rows, int hq, int64_t splits) {
+  const int64_t n = rows * hq * splits;
+  size_t bytes = (size_t)n * D * sizeof(float) + (size_t)n * 2 * sizeof(float);
+  return (bytes + 255) & ~(size_t)255;
+}
+
+int64_t splits_for(int64_t max_len, int split) { return max_len <= 0 ? 1 : (max_len + split - 1) / split; }
+
+CacheView make_view(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
+                    const int32_t* page_table, int max_pages, int window, int32_t* status) {
+  CacheView c;
+  c.pool = static_cast<const uint8_t*>(pool);
+  c.page_bytes = (int64_t)page_bytes_of(g);
+  c.pool_pages = (int64_t)(pool_bytes / (size_t)c.page_bytes);
+  c.ring = static_cast<const __nv_bfloat16*>(ring);
+  c.page_table = page_table;
+  c.max_pages = max_pages;
+  c.num_layers = g->num_layers;
+  c.num_kv_heads = g->num_kv_heads;
+  c.num_q_heads = g->num_q_heads;
+  c.group = g->num_q_heads / g->num_kv_heads;
+  c.layer = layer;
+  c.window = window;
+  c.status = status;
+  return c;
+}
+
+// Checks shared by the attention entry points.
+int check_attn_common(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
+                      int window, const int32_t* page_table, int max_pages, int lanes, const int32_t* seq_len,
+                      int max_seq_len, const void* q, void* workspace, float* out, int32_t* d_status) {
+  int rc = check_geom(g);
+  if (rc) return rc;
+  if (layer < 0 || layer >= g->num_layers || lanes < 0 || max_pages < 0 || max_seq_len < 0) return KVQ_ERR_INVALID_ARG;
+  if (window < 0 || window > P) return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)max_seq_len > (int64_t)max_pages * P) return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)max_pages * P > (int64_t)INT32_MAX) return KVQ_ERR_INVALID_ARG;
+  if (lanes == 0) return KVQ_OK;
+  if (!pool || !page_table || !seq_len || !q || !workspace || !out || !d_status) return KVQ_ERR_INVALID_ARG;
+  if (g->format == KVQ_FMT_HQ2B && !ring) return KVQ_ERR_INVALID_ARG;
+  if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(pool) || !aligned16(ring) || !aligned16(q) || !aligned16(workspace) || !aligned16(out))
+    return KVQ_ERR_ALIGNMENT;
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kvq_page_bytes(const kvq_geom* g) { return check_geom(g) ? 0 : page_bytes_of(g); }
+
+size_t kvq_token_bytes(const kvq_geom* g) { return check_geom(g) ? 0 : page_bytes_of(g) / P; }
+
+size_t kvq_ring_bytes(const kvq_geom* g, int lanes) {
+  if (check_geom(g) || lanes < 0 || g->format != KVQ_FMT_HQ2B) return 0;
+  return (size_t)lanes * g->num_layers * g->num_kv_heads * P * D * 2;
+}
+
+int64_t kvq_pool_pages(const kvq_geom* g, size_t pool_bytes) {
+  if (check_geom(g)) return -1;
+  return (int64_t)(pool_bytes / page_bytes_of(g));
+}
+
+size_t kvq_decode_workspace_bytes(const kvq_geom* g, int lanes, int max_seq_len) {
+  if (check_geom(g) || lanes < 0 || max_seq_len < 0) return 0;
+  return partial_bytes(lanes, g->num_q_heads, splits_for(max_seq_len, decode_split_tokens(g->format)));
+}
+
+size_t kvq_prefill_workspace_bytes(const kvq_geom* g, int n_q_rows, int max_seq_len) {
+  if (check_geom(g) || n_q_rows < 0 || max_seq_len < 0) return 0;
+  return partial_bytes(n_q_rows, g->num_q_heads, splits_for(max_seq_len, prefill_split_tokens(g->format)));
+}
+
+const char* kvq_strerror(int code) {
+  switch (code) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported format or geometry (head_dim 256, page 64, group <= 8)";
+    case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA launch error";
+    case KVQ_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
+    default: return "unknown error";
+  }
+}
+
+int kvq_build_arch(void) { return KVQ_SM; }
+
+int kv_quant_append(const kvq_geom* g, int layer, void* pool, size_t pool_bytes, void* ring,
+                    const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
+                    const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows, const void* k,
+                    const void* v, int32_t* d_status, kvq_stream_t stream) {
+  int rc = check_geom(g);
+  if (rc) return rc;
+  if (layer < 0 || layer >= g->num_layers || lanes < 0 || max_new < 0 || n_rows < 0 || max_pages < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if ((int64_t)max_pages * P > (int64_t)INT32_MAX) return KVQ_ERR_INVALID_ARG;
+  if (lanes == 0 || max_new == 0) return KVQ_OK;
+  if (!pool || !page_table || !start_pos || !n_new || !tok_offset || !k || !v || !d_status)
+    return KVQ_ERR_INVALID_ARG;
+  if (g->format == KVQ_FMT_HQ2B && !ring) return KVQ_ERR_INVALID_ARG;
+  if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(pool) || !aligned16(ring) || !aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
+  CacheView c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, 0, d_status);
+  return launch_append(g->format, c, static_cast<uint8_t*>(pool), static_cast<__nv_bfloat16*>(ring), start_pos,
+                       n_new, tok_offset, max_new, n_rows, lanes, static_cast<const __nv_bfloat16*>(k),
+                       static_cast<const __nv_bfloat16*>(v), (cudaStream_t)stream);
+}
+
+int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
+                      int window, const int32_t* page_table, int max_pages, int lanes, const int32_t* seq_len,
+                      int max_seq_len, const void* q, float sm_scale, void* workspace, size_t ws_bytes,
+                      float* out, int32_t* d_status, kvq_stream_t stream) {
+  int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
+                             max_seq_len, q, workspace, out, d_status);
+  if (rc || lanes == 0) return rc;
+  if (ws_bytes < kvq_decode_workspace_bytes(g, lanes, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  AttnArgs a;
+  a.c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, window, d_status);
+  a.q_pos0 = a.n_q = a.q_offset = nullptr;
+  a.seq_len = seq_len;
+  a.lanes = lanes;
+  a.max_n_q = 1;
+  a.n_q_rows = lanes;
+  a.split_tokens = decode_split_tokens(g->format);
+  a.max_splits = (int)splits_for(max_seq_len, a.split_tokens);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = sm_scale * LOG2E;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = a.ws_o + (int64_t)lanes * g->num_q_heads * a.max_splits * D;
+  a.out = out;
+  if (g->format == KVQ_FMT_HQ2B) return launch_decode_hq2b(a, (cudaStream_t)stream);
+  return launch_attn_generic(g->format, a, 1, (cudaStream_t)stream);
+}
+
+int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
+                       int window, const int32_t* page_table, int max_pages, int lanes, const int32_t* q_pos0,
+                       const int32_t* n_q, const int32_t* q_offset, int max_n_q, int n_q_rows,
+                       const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale, void* workspace,
+                       size_t ws_bytes, float* out, int32_t* d_status, kvq_stream_t stream) {
+  int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
+                             max_seq_len, q, workspace, out, d_status);
+  if (rc) return rc;
+  if (max_n_q < 0 || n_q_rows < 0) return KVQ_ERR_INVALID_ARG;
+  if (lanes == 0 || max_n_q == 0) return KVQ_OK;
+  if (!q_pos0 || !n_q || !q_offset) return KVQ_ERR_INVALID_ARG;
+  if (ws_bytes < kvq_prefill_workspace_bytes(g, n_q_rows, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  AttnArgs a;
+  a.c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, window, d_status);
+  a.q_pos0 = q_pos0;
+  a.n_q = n_q;
+  a.q_offset = q_offset;
+  a.seq_len = seq_len;
+  a.lanes = lanes;
+  a.max_n_q = max_n_q;
+  a.n_q_rows = n_q_rows;
+  a.split_tokens = prefill_split_tokens(g->format);
+  a.max_splits = (int)splits_for(max_seq_len, a.split_tokens);
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = sm_scale * LOG2E;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = a.ws_o + (int64_t)n_q_rows * g->num_q_heads * a.max_splits * D;
+  a.out = out;
+  return launch_attn_generic(g->format, a, 0, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// attn_args.cuh -- arguments of the attention kernels (decode and prefill share them).
+#pragma once
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+struct AttnArgs {
+  CacheView c;
+  const int32_t* q_pos0;    // prefill only
+  const int32_t* n_q;       // prefill only
+  const int32_t* q_offset;  // prefill only
+  const int32_t* seq_len;
+  int lanes, max_n_q, n_q_rows, max_splits, split_tokens;
+  const __nv_bfloat16* q;
+  float scale_log2;  // sm_scale * log2(e)
+  float* ws_o;       // [rows][Hq][max_splits][256]
+  float* ws_ml;      // [rows][Hq][max_splits][2]
+  float* out;        // [rows][Hq][256]
+};
+
+// Resolve query i of lane b: its row, position, and key count.  Returns false (after
+// flagging) when the lane's arguments are invalid or i is past the lane's queries.
+__device__ __forceinline__ bool resolve_query(const AttnArgs& a, bool decode, int b, int i, int& row, int& n_keys,
+                                              int& len, bool flag_errors) {
+  const CacheView& c = a.c;
+  len = a.seq_len[b];
+  if (len < 0 || len > c.max_pages * P) {
+    if (flag_errors) flag(c.status, len < 0 ? KVQ_STATUS_BAD_LEN : KVQ_STATUS_LEN_GT_TABLE);
+    return false;
+  }
+  if (decode) {
+    if (i > 0) return false;
+    row = b;
+    n_keys = len;
+    return true;
+  }
+  const int nq = a.n_q[b], off = a.q_offset[b], pos0 = a.q_pos0[b];
+  if (nq < 0 || nq > a.max_n_q || off < 0 || (int64_t)off + nq > a.n_q_rows || pos0 < 0) {
+    if (flag_errors) flag(c.status, KVQ_STATUS_BAD_LEN);
+    return false;
+  }
+  if (i >= nq) return false;
+  const int pos = pos0 + i;
+  if (pos >= len) {
+    if (flag_errors) flag(c.status, KVQ_STATUS_BAD_LEN);
+    return false;
+  }
+  row = off + i;
+  n_keys = pos + 1;
+  return true;
+}
+
+}  // namespace kvq

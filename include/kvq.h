@@ -1,0 +1,182 @@
+/*
+ * kvq.h -- C ABI of libkvq: GQA attention over a paged KV cache kept in a 2-bit,
+ * 72 B/head/token format (or in BF16 for comparison), hand-written CUDA for sm_103a.
+ *
+ * Sources (web pages; the library follows what they fix and documents what it chose where
+ * they are silent):
+ *   [KV9]  "KV at 9 KB a token" -- sections "How it works" (format table, 64-token pages,
+ *          byte-sized pool) and "The numbers".
+ *   [REUSE] "The KV cache and prompt reuse" -- section "What a sequence is made of" (pages of
+ *          64 tokens shared by all lanes; the window of exact recent keys the compressed
+ *          format keeps) and "Why reuse needs more than the KV pages" (prefix pages shared in
+ *          place, reference counted).
+ *   [HALF] "Half the Cache, Twice the Context" -- table "Two losses with one name" (K scaled
+ *          per channel, V per token) and section "The cliff is in the accumulator, not the
+ *          storage" (two-level accumulation into a real FP32 register).
+ *
+ * Conventions (every entry point):
+ *   - Every pointer argument except `geom` is a DEVICE pointer owned by the caller.  The
+ *     library allocates nothing, never synchronises, and enqueues its kernels on `stream`
+ *     in order (stream-ordered like a cudaMemcpyAsync).
+ *   - Host-detected problems return a negative KVQ_ERR_* code and launch nothing (a format or
+ *     geometry the kernels do not support is refused before any byte moves; there is no CPU
+ *     fallback).  0 means the kernels were enqueued.
+ *   - Device-detected problems (a page id outside the pool, a length past the page table,
+ *     a non-finite or out-of-range input) are OR-ed as KVQ_STATUS_* bits into *d_status
+ *     (device int32; the caller zeroes it and reads it after the stream completes).  The
+ *     unit that met the problem is skipped; the rest of the call proceeds.
+ *   - Alignment: pool, ring, q, k, v, out and workspace must be 16-byte aligned.
+ *   - geom->head_dim must be 256, geom->page_tokens 64, num_q_heads a multiple of
+ *     num_kv_heads with group size G = num_q_heads / num_kv_heads <= 8.
+ *   - Query head j reads KV head j / G (contiguous GQA groups).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kvq_stream_t; /* same handle as cudaStream_t; NULL = legacy stream */
+
+typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1 } kvq_format;
+
+typedef struct {
+  int32_t format;       /* kvq_format */
+  int32_t num_layers;   /* layers that keep a KV cache (16 for the 27B geometry) */
+  int32_t num_kv_heads; /* 4 for the 27B geometry */
+  int32_t num_q_heads;  /* multiple of num_kv_heads, group <= 8 */
+  int32_t head_dim;     /* must be 256 */
+  int32_t page_tokens;  /* must be 64 */
+} kvq_geom;
+
+/* host-side return codes */
+#define KVQ_OK 0
+#define KVQ_ERR_INVALID_ARG (-1)
+#define KVQ_ERR_UNSUPPORTED (-2)
+#define KVQ_ERR_WORKSPACE_TOO_SMALL (-3)
+#define KVQ_ERR_CUDA (-4)
+#define KVQ_ERR_ALIGNMENT (-5)
+
+/* device status bits OR-ed into *d_status */
+#define KVQ_STATUS_PAGE_OOB 1      /* a page-table entry the call needed is outside [0, pool pages) */
+#define KVQ_STATUS_LEN_GT_TABLE 2  /* a position lies past max_pages * 64 */
+#define KVQ_STATUS_BAD_INPUT 4     /* a K/V input is NaN, Inf or |x| > 65504 (not quantized) */
+#define KVQ_STATUS_BAD_LEN 8       /* a negative count, n_new > max_new, rows past n_rows, or a
+                                      prefill query position >= seq_len */
+#define KVQ_STATUS_TIMEOUT 16      /* a bounded wait on a shared-memory barrier gave up */
+
+/*
+ * Pool layout (the format; [KV9] "How it works"):
+ *   The pool is `pool_bytes` of device memory cut into pages of kvq_page_bytes(geom) bytes;
+ *   physical page p starts at byte p * page_bytes.  A page holds 64 tokens of every layer
+ *   and KV head, in blocks ordered [layer][kv_head][K, V].
+ *   KVQ_FMT_HQ2B, block = 4,608 B = 64 tokens x 72 B:
+ *     K block: codes[64 slots][64 B] then scales[256] fp16 (one per channel, written when the
+ *              page closes, i.e. when its slot 63 is appended);
+ *     V block: codes[64 slots][64 B] then meta[64 slots][s0, z0, s1, z1] fp16.
+ *     Code byte b of a 64 B row packs dims 4b..4b+3, dim 4b+j at bits 2j..2j+1.
+ *     V (per token, per 128-dim half h): z = fp16(min), s = fp16((max - min) / 3),
+ *       c = clamp(rint((x - z) / s), 0, 3), c = 0 if s == 0; v^ = z + c s.
+ *     K (per channel d over the 64 keys of a closed page): s_d = fp16(max|x| / 3),
+ *       c = clamp(rint((x / s_d + 3) / 2), 0, 3), c = 2 if s_d == 0; k^ = s_d (2c - 3).
+ *     All steps are IEEE fp32 round-to-nearest-even; rint is half-even.
+ *   KVQ_FMT_BF16, block = 32,768 B: rows[64 slots][256] bf16 for K and for V.
+ *
+ * Ring ([REUSE] "What a sequence is made of": the window of exact recent keys):
+ *   bf16 [lanes][num_layers][num_kv_heads][64 slots][256]; position t of a lane lives in slot
+ *   t % 64.  HQ2B only: keys of the page that is still open exist only here, and attention
+ *   reads key t from the ring iff t >= min(seq_len - window, 64 * floor(seq_len / 64)).
+ *
+ * Page table: int32 [lanes][max_pages] (row stride max_pages); entry i of lane b is the
+ *   physical page of the lane's tokens 64i .. 64i+63.  Several lanes may name the same page
+ *   (a shared prefix, read in place); appending into a shared page is a caller error.
+ */
+
+/* Bytes of one page: num_layers * num_kv_heads * 2 * 64 * (72 | 512).  0 on a bad geom. */
+size_t kvq_page_bytes(const kvq_geom* geom);
+/* Bytes one token costs across all layers and heads, K and V (9,216 / 65,536 at 16 x 4). */
+size_t kvq_token_bytes(const kvq_geom* geom);
+/* Bytes of the exact-key ring for `lanes` lanes (HQ2B; 0 for BF16). */
+size_t kvq_ring_bytes(const kvq_geom* geom, int lanes);
+/* Whole pages a pool of pool_bytes holds; -1 on a bad geom. */
+int64_t kvq_pool_pages(const kvq_geom* geom, size_t pool_bytes);
+/* Workspace paged_decode_attn needs for `lanes` lanes of at most max_seq_len tokens. */
+size_t kvq_decode_workspace_bytes(const kvq_geom* geom, int lanes, int max_seq_len);
+/* Workspace paged_prefill_attn needs for n_q_rows query rows over at most max_seq_len keys. */
+size_t kvq_prefill_workspace_bytes(const kvq_geom* geom, int n_q_rows, int max_seq_len);
+/* Static text for a return code. */
+const char* kvq_strerror(int code);
+/* The SM target the kernels of this build were compiled for (103 for sm_103a). */
+int kvq_build_arch(void);
+
+/*
+ * kv_quant_append -- quantize and append new tokens of one layer ([KV9] "How it works";
+ * [HALF] "Two losses with one name" for the axes).
+ *   For every lane b, rows tok_offset[b] .. tok_offset[b] + n_new[b] - 1 of k and v
+ *   (bf16 [n_rows][num_kv_heads][256]) become positions start_pos[b] .. start_pos[b] +
+ *   n_new[b] - 1 of the lane, placed through page_table.
+ *   HQ2B: each V row is quantized into its page slot; each K row is stored in ring slot
+ *   pos % 64, and every page whose slot 63 is appended by this call is closed: its K block
+ *   is quantized per channel from the page's 64 keys (ring entries for keys appended by
+ *   earlier calls, k rows for the rest).  The resulting bytes do not depend on how a
+ *   sequence is split into calls.  BF16: both rows are stored as they are (ring unused).
+ *   Arguments: layer in [0, num_layers); max_new >= every n_new[b] (host bound that sizes the
+ *   grid); n_rows = rows of k and v; ring may be NULL only for BF16.
+ *   Errors: KVQ_ERR_INVALID_ARG / UNSUPPORTED / ALIGNMENT / CUDA; device bits PAGE_OOB,
+ *   LEN_GT_TABLE, BAD_INPUT (that token/head or page is not written), BAD_LEN.
+ */
+int kv_quant_append(const kvq_geom* geom, int layer, void* pool, size_t pool_bytes, void* ring,
+                    const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
+                    const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows,
+                    const void* k, const void* v, int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * paged_decode_attn -- one query token per lane attends all of the lane's cached tokens
+ * ([KV9] "How it works": attention reads the compressed pages directly, no decompressed
+ * copy; [HALF] "The cliff is in the accumulator": FP32 partials merged once at the end).
+ *   q: bf16 [lanes][num_q_heads][256]; out: fp32 [lanes][num_q_heads][256];
+ *   out[b][j] = sum_t softmax_t(sm_scale * q[b][j] . k^_t) v^_t over t < seq_len[b]
+ *   (seq_len counts the tokens after the step's append).  seq_len[b] == 0 gives zeros.
+ *   window in [0, 64]: the last `window` keys are read exact from the ring (HQ2B).
+ *   max_seq_len (host) >= every seq_len[b] sizes the split-K grid; it must not exceed
+ *   max_pages * 64.  workspace: >= kvq_decode_workspace_bytes(geom, lanes, max_seq_len)
+ *   bytes; its contents on entry are irrelevant (every byte read is first written by the
+ *   same call).
+ *   Errors: KVQ_ERR_*; device bits PAGE_OOB, LEN_GT_TABLE, BAD_LEN, TIMEOUT.
+ */
+int paged_decode_attn(const kvq_geom* geom, int layer, const void* pool, size_t pool_bytes,
+                      const void* ring, int window, const int32_t* page_table, int max_pages,
+                      int lanes, const int32_t* seq_len, int max_seq_len, const void* q,
+                      float sm_scale, void* workspace, size_t ws_bytes, float* out,
+                      int32_t* d_status, kvq_stream_t stream);
+
+/*
+ * paged_prefill_attn -- a chunk of query tokens attends causally over the cache
+ * ([KV9] "How it works": since 0.7.3 prefill attention reads the compressed cache directly;
+ * [KV9] "One cleanup came free": the workspace needs no zeroing).
+ *   The chunk's own K/V must already be appended (kv_quant_append).  For lane b, query rows
+ *   q_offset[b] .. q_offset[b] + n_q[b] - 1 of q (bf16 [n_q_rows][num_q_heads][256]) sit at
+ *   positions q_pos0[b] + i and attend keys 0 .. q_pos0[b] + i (inclusive); out is fp32
+ *   [n_q_rows][num_q_heads][256].  Keys are read from the cache state of seq_len[b] tokens
+ *   (same window rule as decode).  max_n_q (host) >= every n_q[b]; max_seq_len (host) >=
+ *   every seq_len[b]; workspace >= kvq_prefill_workspace_bytes(geom, n_q_rows, max_seq_len),
+ *   contents on entry irrelevant.
+ *   Errors: KVQ_ERR_*; device bits PAGE_OOB, LEN_GT_TABLE, BAD_LEN, TIMEOUT.
+ */
+int paged_prefill_attn(const kvq_geom* geom, int layer, const void* pool, size_t pool_bytes,
+                       const void* ring, int window, const int32_t* page_table, int max_pages,
+                       int lanes, const int32_t* q_pos0, const int32_t* n_q,
+                       const int32_t* q_offset, int max_n_q, int n_q_rows,
+                       const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale,
+                       void* workspace, size_t ws_bytes, float* out, int32_t* d_status,
+                       kvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

@@ -1,0 +1,130 @@
+"""The C ABI library loads, exports every symbol include/kvq.h declares, sizes buffers as the
+format says, and rejects bad calls on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from compressed_paged_kv_quant_gb300 import build, kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return kvq.lib()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return set(re.findall(r"\b([a-z_0-9]+)\s*\([^;{]*\)\s*;", src))
+
+
+def test_every_declared_symbol_is_exported(L):
+    declared = _declared()
+    assert {"kv_quant_append", "paged_decode_attn", "paged_prefill_attn"} <= declared
+    assert declared == set(kvq.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_build_targets_sm103(L):
+    assert L.kvq_build_arch() == 103
+
+
+def test_sizes_27b_geometry(L):
+    gh = kvq.geom(kvq.FMT_HQ2B, 16, 4, 24)
+    gb = kvq.geom(kvq.FMT_BF16, 16, 4, 24)
+    assert kvq.token_bytes(gh) == 9216 and kvq.token_bytes(gb) == 65536
+    assert kvq.page_bytes(gh) == 64 * 9216
+    assert kvq.pool_pages(gh, 8 * 40960 * 9216) == 5120
+    assert kvq.ring_bytes(gh, 8) == 8 * 16 * 4 * 64 * 256 * 2
+    assert kvq.ring_bytes(gb, 8) == 0
+    # decode: 8 lanes x 24 heads x 40 splits x (256 + 2) floats
+    assert kvq.decode_workspace_bytes(gh, 8, 40960) >= 8 * 24 * 40 * 258 * 4
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=128), dict(page_tokens=32), dict(format=7),
+                                 dict(num_q_heads=36), dict(num_q_heads=10)])
+def test_unsupported_geometry_is_refused(L, bad):
+    args = dict(format=0, num_layers=16, num_kv_heads=4, num_q_heads=24, head_dim=256, page_tokens=64)
+    args.update(bad)
+    g = kvq.Geom(**args)
+    assert kvq.page_bytes(g) == 0
+    assert kvq.pool_pages(g, 1 << 30) == -1
+    rc = L.paged_decode_attn(ctypes.byref(g), 0, 16, 1 << 20, 16, 0, 16, 1, 1, 16, 64, 16, 0.0625, 16,
+                             1 << 20, 16, 16, None)
+    assert rc in (kvq.ERR_UNSUPPORTED, kvq.ERR_INVALID_ARG)
+
+
+def _decode(L, g, **kw):
+    a = dict(layer=0, pool=256, pool_bytes=1 << 24, ring=512, window=0, pt=768, max_pages=4, lanes=1,
+             seq_len=1024, max_seq_len=256, q=1280, scale=0.0625, ws=1536, ws_bytes=1 << 24, out=1792,
+             status=2048)
+    a.update(kw)
+    return L.paged_decode_attn(ctypes.byref(g), a["layer"], a["pool"], a["pool_bytes"], a["ring"], a["window"],
+                               a["pt"], a["max_pages"], a["lanes"], a["seq_len"], a["max_seq_len"], a["q"],
+                               a["scale"], a["ws"], a["ws_bytes"], a["out"], a["status"], None)
+
+
+def test_decode_host_validation(L):
+    g = kvq.geom(kvq.FMT_HQ2B, 2, 1, 4)
+    assert _decode(L, g, layer=2) == kvq.ERR_INVALID_ARG
+    assert _decode(L, g, layer=-1) == kvq.ERR_INVALID_ARG
+    assert _decode(L, g, window=65) == kvq.ERR_INVALID_ARG
+    assert _decode(L, g, max_seq_len=257) == kvq.ERR_INVALID_ARG     # past max_pages * 64
+    assert _decode(L, g, ring=None) == kvq.ERR_INVALID_ARG           # 2-bit needs the ring
+    assert _decode(L, g, q=None) == kvq.ERR_INVALID_ARG
+    assert _decode(L, g, pool_bytes=100) == kvq.ERR_INVALID_ARG      # smaller than one page
+    assert _decode(L, g, q=1288) == kvq.ERR_ALIGNMENT
+    assert _decode(L, g, ws_bytes=64) == kvq.ERR_WORKSPACE_TOO_SMALL
+    assert _decode(L, g, lanes=0) == kvq.OK                           # nothing to do, nothing launched
+
+
+def test_append_host_validation(L):
+    g = kvq.geom(kvq.FMT_HQ2B, 1, 1, 4)
+
+    def app(**kw):
+        a = dict(layer=0, pool=256, pool_bytes=1 << 20, ring=512, pt=768, max_pages=4, lanes=1, start=1024,
+                 n=1040, off=1056, max_new=64, n_rows=64, k=1280, v=1536, status=2048)
+        a.update(kw)
+        return L.kv_quant_append(ctypes.byref(g), a["layer"], a["pool"], a["pool_bytes"], a["ring"], a["pt"],
+                                 a["max_pages"], a["lanes"], a["start"], a["n"], a["off"], a["max_new"],
+                                 a["n_rows"], a["k"], a["v"], a["status"], None)
+
+    assert app(layer=1) == kvq.ERR_INVALID_ARG
+    assert app(max_new=-1) == kvq.ERR_INVALID_ARG
+    assert app(ring=None) == kvq.ERR_INVALID_ARG
+    assert app(k=None) == kvq.ERR_INVALID_ARG
+    assert app(v=1544) == kvq.ERR_ALIGNMENT
+    assert app(max_new=0) == kvq.OK
+    gb = kvq.geom(kvq.FMT_BF16, 1, 1, 4)
+    assert L.kv_quant_append(ctypes.byref(gb), 0, 256, 1 << 20, None, 768, 4, 1, 1024, 1040, 1056, 0, 0,
+                             1280, 1536, 2048, None) == kvq.OK
+
+
+def test_prefill_host_validation(L):
+    g = kvq.geom(kvq.FMT_BF16, 1, 1, 4)
+
+    def pre(**kw):
+        a = dict(pool=256, pool_bytes=1 << 22, pt=768, max_pages=4, lanes=1, qp=1024, nq=1040, qo=1056,
+                 max_n_q=16, rows=16, seq=1072, max_seq=256, q=1280, ws=1536, ws_bytes=1 << 24, out=1792,
+                 status=2048)
+        a.update(kw)
+        return L.paged_prefill_attn(ctypes.byref(g), 0, a["pool"], a["pool_bytes"], None, 0, a["pt"],
+                                    a["max_pages"], a["lanes"], a["qp"], a["nq"], a["qo"], a["max_n_q"],
+                                    a["rows"], a["seq"], a["max_seq"], a["q"], 0.0625, a["ws"], a["ws_bytes"],
+                                    a["out"], a["status"], None)
+
+    assert pre(qp=None) == kvq.ERR_INVALID_ARG
+    assert pre(max_n_q=-1) == kvq.ERR_INVALID_ARG
+    assert pre(ws_bytes=1024) == kvq.ERR_WORKSPACE_TOO_SMALL
+    assert pre(max_n_q=0) == kvq.OK
+
+
+def test_strerror(L):
+    for code in (0, -1, -2, -3, -4, -5, -99):
+        assert isinstance(kvq.strerror(code), str) and kvq.strerror(code)

@@ -1,0 +1,258 @@
+"""GPU path vs the CPU oracle on small, seeded workloads that span several pages, splits and
+ragged tails: bit-exact pool and ring bytes after append, attention within tolerance."""
+import numpy as np
+import pytest
+
+import oracle
+from compressed_paged_kv_quant_gb300 import synth
+from oracle_side import assert_close, host_kv
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+HQ, BF = oracle.FMT_HQ2B, oracle.FMT_BF16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_paged_kv_quant_gb300 import build
+    build.build()
+
+
+def _dw(wl, fmt, fill=0xA5):
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+    return DeviceWorkload(wl, fmt, "cuda", fill)
+
+
+def _u16(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _custom(lens, L=1, H=1, Hq=4, seed=0, window=0, extra_pages=3, k_out=True, v_out=True):
+    pages = [(n + 63) // 64 for n in lens]
+    total = sum(pages) + extra_pages
+    perm = synth.permutation(seed, total, salt=7)
+    rows, off = [], 0
+    for p in pages:
+        rows.append(perm[off:off + p])
+        off += p
+    mp = max(max(pages), 1)
+    t = np.full((len(lens), mp), -1, np.int32)
+    for b, r in enumerate(rows):
+        t[b, :len(r)] = r
+    return synth.Workload(f"custom_{lens}", L, H, Hq, list(lens), t, total, window=window, seed=seed,
+                          k_outliers=k_out, v_outliers=v_out)
+
+
+def _oracle_full(wl, fmt, layers=None, fill=0xA5):
+    """Oracle pool/ring with the workload's own geometry and page table, every lane filled."""
+    g = oracle.geom(fmt, wl.num_layers, wl.num_kv_heads, wl.num_q_heads)
+    pool = np.full(wl.pool_pages * oracle.page_bytes(g), fill, np.uint8)
+    ring = np.zeros((wl.lanes, wl.num_layers, wl.num_kv_heads, 64, 256), np.uint16)
+    for layer in (range(wl.num_layers) if layers is None else layers):
+        for b, n in enumerate(wl.seq_len):
+            k = host_kv(wl, layer, b, 0, n, 0)
+            v = host_kv(wl, layer, b, 0, n, 1)
+            pt = np.ascontiguousarray(wl.page_table[b:b + 1])
+            ring_b = np.ascontiguousarray(ring[b:b + 1])
+            gl = g
+            st = oracle.append(gl, layer, pool, ring_b, pt, 1, [0], [n], [0], k, v)
+            assert st == 0
+            ring[b] = ring_b[0]
+    return g, pool, ring
+
+
+def _gpu_fill(dw, chunking="one"):
+    wl = dw.wl
+    rng = np.random.default_rng(1)
+    for layer in range(wl.num_layers):
+        if chunking == "one":
+            dw.fill_history(wl.seq_len, layers=[layer], chunk=1 << 20)
+            continue
+        # batched ragged calls: every call appends a random count to every lane
+        pos = [0] * wl.lanes
+        while any(p < n for p, n in zip(pos, wl.seq_len)):
+            lanes, starts, counts, ks, vs = [], [], [], [], []
+            for b, n in enumerate(wl.seq_len):
+                if pos[b] >= n:
+                    continue
+                c = 1 if chunking == "tokens" else int(rng.integers(1, 150))
+                c = min(c, n - pos[b])
+                lanes.append(b)
+                starts.append(pos[b])
+                counts.append(c)
+                ks.append(wl.kv_torch(layer, b, pos[b], c, 0, "cuda"))
+                vs.append(wl.kv_torch(layer, b, pos[b], c, 1, "cuda"))
+                pos[b] += c
+            dw.append(layer, lanes, starts, counts, torch.cat(ks), torch.cat(vs))
+    torch.cuda.synchronize()
+
+
+def test_device_generator_matches_host():
+    wl = synth.tiny_decode()
+    for kv in (0, 1):
+        a = _u16(wl.kv_torch(0, 0, 0, 256, kv, "cuda"))
+        np.testing.assert_array_equal(a, wl.kv_np(0, 0, 0, 256, kv))
+    np.testing.assert_array_equal(_u16(wl.q_torch(0, 0, 255, 1, "cuda")), wl.q_np(0, 0, 255, 1))
+
+
+@pytest.mark.parametrize("window", [0, 64])
+def test_tiny_decode_bytes_and_output(window):
+    """The tiny decode step: 1 layer, 1 KV head, GQA 4, 256 tokens on 4 scattered pages."""
+    wl = synth.tiny_decode()
+    dw = _dw(wl, HQ)
+    _gpu_fill(dw)
+    g, pool, ring = _oracle_full(wl, HQ)
+    np.testing.assert_array_equal(dw.cache.pool.cpu().numpy(), pool)
+    np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
+    q = dw.step_q(0)
+    ws, out = dw.decode_buffers()
+    ws.view(torch.int32).fill_(-1)                       # garbage: NaN bit patterns everywhere
+    dw.decode(0, q, ws, out, window=window)
+    assert dw.cache.read_status() == 0
+    ref, st = oracle.decode(g, 0, pool, ring, window, wl.page_table, 1, wl.seq_len, wl.q_np(0, 0, 255, 1),
+                            dw.sm_scale)
+    assert st == 0
+    assert_close(out.cpu().numpy(), ref, what="tiny decode")
+
+
+@pytest.mark.parametrize("chunking", ["one", "tokens", "random"])
+def test_append_bytes_independent_of_chunking(chunking):
+    wl = _custom([300, 129, 64, 5], L=2, H=2, Hq=4)
+    dw = _dw(wl, HQ)
+    _gpu_fill(dw, chunking)
+    assert dw.cache.read_status() == 0
+    g, pool, ring = _oracle_full(wl, HQ)
+    np.testing.assert_array_equal(dw.cache.pool.cpu().numpy(), pool)
+    np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
+
+
+def test_bf16_append_bytes():
+    wl = _custom([200, 64, 1], L=2, H=2, Hq=4)
+    dw = _dw(wl, BF)
+    _gpu_fill(dw, "random")
+    g, pool, _ = _oracle_full(wl, BF)
+    np.testing.assert_array_equal(dw.cache.pool.cpu().numpy(), pool)
+
+
+LENS = [1, 63, 64, 65, 700, 1500, 2049, 3000]
+
+
+@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (HQ, 17), (BF, 0)])
+def test_decode_ragged_lanes(fmt, window):
+    wl = _custom(LENS, L=2, H=2, Hq=12, window=window)
+    dw = _dw(wl, fmt)
+    _gpu_fill(dw)
+    g, pool, ring = _oracle_full(wl, fmt)
+    ws, out = dw.decode_buffers()
+    for layer in range(2):
+        ws.view(torch.int32).fill_(0x7FC00001)
+        q = dw.step_q(layer)
+        dw.decode(layer, q, ws, out)
+        qh = np.concatenate([wl.q_np(layer, b, n - 1, 1) for b, n in enumerate(LENS)])
+        ref, st = oracle.decode(g, layer, pool, ring if fmt == HQ else None, window, wl.page_table, wl.lanes,
+                                LENS, qh, dw.sm_scale)
+        assert st == 0
+        assert_close(out.cpu().numpy(), ref, what=f"decode fmt={fmt} W={window} layer={layer}")
+    assert dw.cache.read_status() == 0
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 7, 8])
+def test_decode_group_sizes(G):
+    lens = [333, 1100]
+    wl = _custom(lens, L=1, H=2, Hq=2 * G)
+    dw = _dw(wl, HQ)
+    _gpu_fill(dw)
+    g, pool, ring = _oracle_full(wl, HQ)
+    ws, out = dw.decode_buffers()
+    dw.decode(0, dw.step_q(0), ws, out)
+    qh = np.concatenate([wl.q_np(0, b, n - 1, 1) for b, n in enumerate(lens)])
+    ref, _ = oracle.decode(g, 0, pool, ring, 0, wl.page_table, 2, lens, qh, dw.sm_scale)
+    assert_close(out.cpu().numpy(), ref, what=f"G={G}")
+
+
+def test_decode_zero_length_lane_gives_zeros():
+    wl = _custom([130, 0, 64], L=1, H=1, Hq=4)
+    dw = _dw(wl, HQ)
+    dw.fill_history([130, 0, 64])
+    ws, out = dw.decode_buffers()
+    out.fill_(7.0)
+    q = torch.cat([wl.q_torch(0, b, max(n - 1, 0), 1, "cuda") for b, n in enumerate(wl.seq_len)])
+    dw.decode(0, q, ws, out)
+    assert dw.cache.read_status() == 0
+    assert torch.all(out[1] == 0)
+    assert torch.all(torch.isfinite(out))
+
+
+@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (BF, 0)])
+def test_prefill_chunks(fmt, window):
+    """Causal chunks over a compressed prefix: (prefix, chunk) = (300, 100), (0, 70), (1000, 1100)."""
+    prefix, chunk = [300, 0, 1000], [100, 70, 1100]
+    lens = [p + c for p, c in zip(prefix, chunk)]
+    wl = _custom(lens, L=2, H=2, Hq=12, window=window)
+    dw = _dw(wl, fmt)
+    _gpu_fill(dw)            # prefix and chunk K/V appended (the chunk's own K/V first, as required)
+    g, pool, ring = _oracle_full(wl, fmt)
+    rows = sum(chunk)
+    ws, out = dw.prefill_buffers(rows)
+    offs = np.cumsum([0] + chunk[:-1]).tolist()
+    for layer in range(2):
+        ws.view(torch.int32).fill_(-1)
+        q = torch.cat([wl.q_torch(layer, b, prefix[b], chunk[b], "cuda") for b in range(3)])
+        dw.prefill(layer, q, prefix, chunk, offs, ws, out)
+        qh = np.concatenate([wl.q_np(layer, b, prefix[b], chunk[b]) for b in range(3)])
+        ref, st = oracle.prefill(g, layer, pool, ring if fmt == HQ else None, window, wl.page_table, 3, prefix,
+                                 chunk, offs, lens, qh, dw.sm_scale)
+        assert st == 0
+        assert_close(out.cpu().numpy(), ref, what=f"prefill fmt={fmt} W={window} layer={layer}")
+    assert dw.cache.read_status() == 0
+
+
+def test_device_status_flags():
+    from compressed_paged_kv_quant_gb300 import kvq
+    wl = _custom([200], L=1, H=1, Hq=4)
+    dw = _dw(wl, HQ)
+    dw.fill_history([200])
+    torch.cuda.synchronize()
+    assert dw.cache.read_status() == 0
+    # a page id outside the pool inside the length
+    saved = dw.page_table.clone()
+    dw.page_table[0, 1] = wl.pool_pages + 5
+    ws, out = dw.decode_buffers()
+    dw.decode(0, dw.step_q(0), ws, out)
+    assert dw.cache.read_status() & kvq.STATUS_PAGE_OOB
+    dw.page_table.copy_(saved)
+    dw.cache.clear_status()
+    # a NaN input is flagged and not quantized
+    k = wl.kv_torch(0, 0, 200, 1, 0, "cuda")
+    k[0, 0, 3] = float("nan")
+    v = wl.kv_torch(0, 0, 200, 1, 1, "cuda")
+    dw.append(0, [0], [199], [1], k, v)
+    assert dw.cache.read_status() & kvq.STATUS_BAD_INPUT
+    dw.cache.clear_status()
+    # a count beyond max_new
+    kvq.kv_quant_append(dw.g, 0, dw.cache.pool, dw.cache.ring, dw.page_table,
+                        torch.tensor([0], dtype=torch.int32, device="cuda"),
+                        torch.tensor([5], dtype=torch.int32, device="cuda"),
+                        torch.tensor([0], dtype=torch.int32, device="cuda"), 2, k.repeat(5, 1, 1),
+                        v.repeat(5, 1, 1), dw.cache.status)
+    assert dw.cache.read_status() & kvq.STATUS_BAD_LEN
+
+
+def test_flat_attention_over_131072_keys_keeps_full_mass():
+    """q = 0 gives a flat softmax over 131,072 keys: the output must be the mean of the
+    values.  With an accumulator rounded to bf16 after every add the weights would sum to
+    0.001953 ("Half the Cache", accumulator table); the FP32 two-level path keeps 1.0."""
+    n = 131072
+    wl = _custom([n], L=1, H=1, Hq=4, extra_pages=0)
+    dw = _dw(wl, HQ)
+    _gpu_fill(dw)
+    g, pool, ring = _oracle_full(wl, HQ)
+    q = torch.zeros((1, 4, 256), dtype=torch.bfloat16, device="cuda")
+    ws, out = dw.decode_buffers()
+    dw.decode(0, q, ws, out)
+    o = out.cpu().numpy()
+    ref, _ = oracle.decode(g, 0, pool, ring, 0, wl.page_table, 1, [n], np.zeros((1, 4, 256), np.uint16), 1.0)
+    assert_close(o, ref, atol=1e-5, rtol=1e-5, what="flat 131072")
