@@ -1,0 +1,367 @@
+#!/usr/bin/env python3
+"""Benchmark: batched decode over the 2-bit paged KV cache at the 27B geometry.
+
+Workload (one step): 16 layers x 4 KV heads x head_dim 256, 24 query heads (GQA 6), 8 lanes
+at a 40,960-token context after the step's append, pages scattered through one byte-sized
+pool (8 x 40,960 x 9,216 B).  For every layer the step quantize-appends each lane's new
+token (kv_quant_append) and runs paged_decode_attn for one query token per lane.  The step
+is captured once in a CUDA graph and replayed.
+
+Printed: one JSON line.  `value` = context tokens attended per second (lanes x 40,960 per
+16-layer step, inputs resident in HBM); `e2e` = the same with the step's q/k/v copied from
+pinned host memory and the outputs copied back inside the timed region; `roofline` = the
+attention call's compressed-KV bytes over its CUDA-event duration against the measured HBM
+copy bandwidth; `cpu_baseline` = the CPU oracle on a bounded sample of the same step.
+
+`--impl reference` times the CPU oracle alone (the reference arm for this workload).
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(lanes=8, ctx=40960, layers=16, kv_heads=4, q_heads=24)
+METRIC = "decode attn: compressed-KV tokens/s & achieved HBM GB/s (% of peak); prefill TFLOP/s"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _config(extra=None):
+    c = {"workload": "decode_27b_8x40960: 16 layers x 4 KV heads x 256, 24 q heads, 8 lanes x 40,960 tokens, "
+                     "2-bit pages (72 B/head/token), append + decode per layer",
+         "lanes": WORKLOAD["lanes"], "context_tokens": WORKLOAD["ctx"], "layers": WORKLOAD["layers"],
+         "kv_heads": WORKLOAD["kv_heads"], "q_heads": WORKLOAD["q_heads"], "head_dim": 256, "page_tokens": 64,
+         "pool_bytes": WORKLOAD["lanes"] * WORKLOAD["ctx"] * 9216,
+         "l2_policy": "inputs larger than L2 (3.02 GB pool read per step)",
+         "parallelism": "replicas only (one GPU per process)"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+# ----------------------------------------------------------------------------- clocks
+class Clocks:
+    def __init__(self):
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-i", str(_device_index())],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx = max(mx, float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        except Exception:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _device_index():
+    v = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if v:
+        ids = [x for x in v.split(",") if x.strip()]
+        if local < len(ids) and ids[local].strip().isdigit():
+            return int(ids[local])
+    return local
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+class OracleDecode:
+    """The CPU oracle on lane 0 of the workload, layer 0's cache: set up once (host inputs,
+    history appended, untimed), then timed per lane-layer decode (append of the step token +
+    fp64 attention of all 24 query heads over the lane's 40,960 tokens).  The oracle's cost
+    does not depend on the values, so one layer's cache stands in for every layer."""
+
+    def __init__(self, seed=0, threads=None):
+        import numpy as np
+
+        import oracle
+        from compressed_paged_kv_quant_gb300 import synth
+        self.oracle = oracle
+        wl = synth.batched_decode_27b(seed=seed)
+        self.wl, self.n = wl, wl.seq_len[0]
+        n = self.n
+        self.g = oracle.geom(oracle.FMT_HQ2B, 1, wl.num_kv_heads, wl.num_q_heads)
+        npg = n // 64
+        self.pool = np.zeros(npg * oracle.page_bytes(self.g), np.uint8)
+        self.ring = np.zeros((1, 1, wl.num_kv_heads, 64, 256), np.uint16)
+        self.pt = np.arange(npg, dtype=np.int32)[None, :]
+        self.k = synth.kv_np_parallel(wl, 0, 0, 0, n, 0)
+        self.v = synth.kv_np_parallel(wl, 0, 0, 0, n, 1)
+        assert oracle.append(self.g, 0, self.pool, self.ring, self.pt, 1, [0], [n - 1], [0], self.k, self.v) == 0
+        self.q = wl.q_np(0, 0, n - 1, 1)[0]
+        self.threads = threads or max(1, min(os.cpu_count() or 1, wl.num_q_heads))
+
+    def run(self, repeats):
+        """Seconds for `repeats` lane-layer decode steps."""
+        o, n = self.oracle, self.n
+        heads = range(self.wl.num_q_heads)
+        t0 = time.perf_counter()
+        with cf.ThreadPoolExecutor(self.threads) as ex:
+            for _ in range(repeats):
+                assert o.append(self.g, 0, self.pool, self.ring, self.pt, 1, [n - 1], [1], [n - 1], self.k, self.v) == 0
+                list(ex.map(lambda j: o.attend(self.g, 0, self.pool, self.ring, 0, self.pt[0], 0, n, j, self.q[j], n,
+                                               0.0625), heads))
+        return time.perf_counter() - t0
+
+    def value(self, repeats, seconds):
+        """Context tokens per second in the benchmark's unit (16-layer steps)."""
+        return repeats * self.n / self.wl.num_layers / seconds
+
+    def describe(self, repeats):
+        return (f"lane 0 of 8, {repeats} lane-layer decode steps on layer 0's cache (append of the step token + "
+                f"fp64 attention of all {self.wl.num_q_heads} query heads over {self.n} tokens), {self.threads} "
+                f"threads; scaled to 16-layer steps (context tokens per second)")
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores; one step = one lane
+    through all 16 layers (16 lane-layer decodes)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    od = OracleDecode(seed=args.seed)
+    per_step = od.wl.num_layers
+    for _ in range(args.warmup):
+        od.run(1)
+    secs = [od.run(per_step) for _ in range(args.steps)]
+    value = od.value(per_step * args.steps, sum(secs))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * WORKLOAD["lanes"] * WORKLOAD["ctx"] / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": od.threads, "kind": "oracle",
+                             "sample": od.describe(per_step) + f" per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from compressed_paged_kv_quant_gb300 import build, kvq, synth
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+
+    wl = synth.batched_decode_27b(seed=args.seed + rank, lanes=args.lanes, ctx=args.ctx, layers=args.layers)
+    L, lanes, ctx = wl.num_layers, wl.lanes, wl.seq_len[0]
+    H, Hq = wl.num_kv_heads, wl.num_q_heads
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        dw = DeviceWorkload(wl, kvq.FMT_HQ2B, dev, fill=None, stream=stream.cuda_stream)
+        dw.fill_history([n - 1 for n in wl.seq_len], chunk=16384)
+        # one contiguous input buffer (q, k, v of every layer) and one output buffer per step
+        n_q, n_kv = lanes * Hq * 256, lanes * H * 256
+        step_in = torch.empty(L * (n_q + 2 * n_kv), dtype=torch.bfloat16, device=dev)
+        q_v, k_v, v_v = [], [], []
+        for l in range(L):
+            base = l * (n_q + 2 * n_kv)
+            q_v.append(step_in[base:base + n_q].view(lanes, Hq, 256))
+            k_v.append(step_in[base + n_q:base + n_q + n_kv].view(lanes, H, 256))
+            v_v.append(step_in[base + n_q + n_kv:base + n_q + 2 * n_kv].view(lanes, H, 256))
+            q_v[l].copy_(dw.step_q(l))
+            k, v = dw.step_kv(l)
+            k_v[l].copy_(k)
+            v_v[l].copy_(v)
+        ws, _ = dw.decode_buffers()
+        step_out = torch.empty((L, lanes, Hq, 256), dtype=torch.float32, device=dev)
+    stream.synchronize()
+    assert dw.cache.read_status() == 0
+
+    def step():
+        for l in range(L):
+            dw.append_step(l, k_v[l], v_v[l])
+            dw.decode(l, q_v[l], ws, step_out[l])
+
+    # capture one step in a CUDA graph
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    stream.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            g.replay()
+    barrier()
+    clocks = Clocks()
+    clocks.start()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert dw.cache.read_status() == 0, "device status flagged during the timed steps"
+    tokens_per_step = lanes * ctx
+    value = world * tokens_per_step / (ms / 1000.0)
+
+    # per-call duration of the attention (CUDA events on the launching stream, same inputs)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    call_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.steps)):
+            for l in range(L):
+                ev[l][0].record(stream)
+                dw.decode(l, q_v[l], ws, step_out[l])
+                ev[l][1].record(stream)
+            stream.synchronize()
+            call_ms += [x.elapsed_time(y) for x, y in ev]
+    call_ms = statistics.median(call_ms)
+    attn_bytes = lanes * ctx * H * 144          # compressed K+V bytes one layer's attention reads
+    peak, peak_src = _peaks()
+    achieved = attn_bytes / (call_ms / 1000.0) / 1e9
+
+    # end to end: the step's q/k/v from pinned host memory, outputs back to pinned host memory
+    h_in = step_in.cpu().pin_memory()
+    h_out = torch.empty(step_out.shape, dtype=step_out.dtype, pin_memory=True)
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        step_in.copy_(h_in, non_blocking=True)
+        g.replay()
+        h_out.copy_(step_out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+    barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * tokens_per_step / (e2e_ms / 1000.0)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        od = OracleDecode(seed=args.seed)
+        od.run(1)
+        dt = od.run(args.cpu_repeats)
+        cpu = {"value": od.value(args.cpu_repeats, dt), "unit": UNIT, "cores": od.threads, "kind": "oracle",
+               "sample": od.describe(args.cpu_repeats), "seconds": round(dt, 2)}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (2-bit codes)", "data": "synthetic",
+                "config": _config({"ms_per_attention_call": call_ms, "peak_source": peak_src}),
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak, "traffic": None,
+                             "kernel": "paged_decode_attn (decode_hq2b_main + decode_hq2b_combine), one layer",
+                             "algorithmic_bytes_per_launch": attn_bytes},
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": 4 * L * args.steps,
+                "clocks": clk}
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-repeats", type=int, default=64,
+                    help="oracle decodes of one lane-layer timed for the CPU baseline")
+    # smaller cases of the same workload, for profiling only (the defaults are the benchmark)
+    ap.add_argument("--lanes", type=int, default=WORKLOAD["lanes"])
+    ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
+    ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -14,6 +14,9 @@ int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t str
 int launch_decode_hq2b(const AttnArgs& a, cudaStream_t stream);
 int decode_split_tokens(int fmt);
 int prefill_split_tokens(int fmt);
+int decode_hq2b_slots(int max_seq_len);
+int launch_prefill_hq2b_tc(const AttnArgs& a, cudaStream_t stream);
+int launch_attn_combine(const AttnArgs& a, int decode, cudaStream_t stream);
 }  // namespace kvq
 
 #include "attn_args.cuh"
@@ -48,6 +51,11 @@ size_t partial_bytes(int64_t rows, int hq, int64_t splits) {
 }
 
 int64_t splits_for(int64_t max_len, int split) { return max_len <= 0 ? 1 : (max_len + split - 1) / split; }
+
+// partial records per (lane, query head) the decode kernels may write
+int64_t decode_slots(int fmt, int max_seq_len) {
+  return fmt == KVQ_FMT_HQ2B ? decode_hq2b_slots(max_seq_len) : splits_for(max_seq_len, decode_split_tokens(fmt));
+}
 
 CacheView make_view(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
                     const int32_t* page_table, int max_pages, int window, int32_t* status) {
@@ -107,7 +115,7 @@ int64_t kvq_pool_pages(const kvq_geom* g, size_t pool_bytes) {
 
 size_t kvq_decode_workspace_bytes(const kvq_geom* g, int lanes, int max_seq_len) {
   if (check_geom(g) || lanes < 0 || max_seq_len < 0) return 0;
-  return partial_bytes(lanes, g->num_q_heads, splits_for(max_seq_len, decode_split_tokens(g->format)));
+  return partial_bytes(lanes, g->num_q_heads, decode_slots(g->format, max_seq_len));
 }
 
 size_t kvq_prefill_workspace_bytes(const kvq_geom* g, int n_q_rows, int max_seq_len) {
@@ -166,7 +174,10 @@ int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t poo
   a.max_n_q = 1;
   a.n_q_rows = lanes;
   a.split_tokens = decode_split_tokens(g->format);
-  a.max_splits = (int)splits_for(max_seq_len, a.split_tokens);
+  a.max_splits = (int)decode_slots(g->format, max_seq_len);
+  a.grid_warps = 0;
+  a.min_wp = 0;
+  a.max_seq_len = max_seq_len;
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.scale_log2 = sm_scale * LOG2E;
   a.ws_o = static_cast<float*>(workspace);
@@ -204,6 +215,13 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
   a.ws_o = static_cast<float*>(workspace);
   a.ws_ml = a.ws_o + (int64_t)n_q_rows * g->num_q_heads * a.max_splits * D;
   a.out = out;
+  a.grid_warps = 0;
+  a.min_wp = 0;
+  a.max_seq_len = max_seq_len;
+  if (g->format == KVQ_FMT_HQ2B) {
+    rc = launch_prefill_hq2b_tc(a, (cudaStream_t)stream);
+    return rc ? rc : launch_attn_combine(a, 0, (cudaStream_t)stream);
+  }
   return launch_attn_generic(g->format, a, 0, (cudaStream_t)stream);
 }
 

@@ -16,6 +16,9 @@ struct AttnArgs {
   float* ws_o;       // [rows][Hq][max_splits][256]
   float* ws_ml;      // [rows][Hq][max_splits][2]
   float* out;        // [rows][Hq][256]
+  int grid_warps;    // fast 2-bit decode: warps of the persistent grid
+  int min_wp;        // fast 2-bit decode: least pages per warp (bounds the partials per lane/head)
+  int max_seq_len;   // host bound on every seq_len[b]
 };
 
 // Resolve query i of lane b: its row, position, and key count.  Returns false (after

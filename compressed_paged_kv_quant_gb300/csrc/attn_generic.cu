@@ -173,6 +173,13 @@ __global__ void __launch_bounds__(256) attn_combine(AttnArgs a, int decode, int 
 int decode_split_tokens(int fmt) { return fmt == KVQ_FMT_HQ2B ? DECODE_SPLIT_HQ2B : GENERIC_SPLIT; }
 int prefill_split_tokens(int) { return PREFILL_SPLIT; }
 
+int launch_attn_combine(const AttnArgs& a, int decode, cudaStream_t stream) {
+  const int rows = decode ? 1 : a.max_n_q;
+  dim3 cg(a.lanes * rows, a.c.num_q_heads);
+  attn_combine<<<cg, 256, 0, stream>>>(a, decode, a.split_tokens);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t stream) {
   const int warps = decode ? 1 : 4;
   const int rows = decode ? 1 : a.max_n_q;

@@ -1,0 +1,510 @@
+// prefill_tc.cu -- chunked-prefill attention over the 2-bit pages on the 5th-generation
+// tensor cores (tcgen05, TMEM accumulators), sm_103a.
+//
+// "KV at 9 KB a token" ("How it works"): since 0.7.3 prefill attention reads the compressed
+// cache directly -- no decompressed copy of the prompt exists in HBM.  Here each 64-token page
+// is dequantised once into shared memory, where it feeds the MMAs of 128 query rows.  The
+// split partials are written before they are read, so the workspace is never zeroed ("One
+// cleanup came free with the format").
+//
+// CTA = up to 128 rows of (query, head) pairs of one GQA group (row = qi * G + g) x one key
+// split of `split_tokens` keys.
+//   TMEM (512 columns):  Q [0,128) as fp16 pairs (A operand of S = Q K^T);
+//                        S/P double buffer [128,192) [192,256): S lands in fp32, P is written
+//                        back over its first 32 columns as fp16 pairs (A operand of O += P V);
+//                        O [256,512) fp32 accumulator of the split.
+//   Shared memory:       K tile x2 (64 keys x 256 dims fp16, 128B-swizzled K-major = B of S),
+//                        V^T tile x2 (256 dims x 64 keys fp16, 128B-swizzled K-major = B of PV),
+//                        compressed-page staging x2 (one 9,216 B TMA bulk copy per page).
+//   Warps 0-3: softmax, one row per thread (= TMEM lane): S from TMEM, causal mask, online
+//              max with lazy O rescale (only when a row max grows by more than 2^8), P to
+//              TMEM, l in FP32; the epilogue writes (m, l, O) of the split.
+//   Warps 4-7: page TMA (one elected thread) and dequantisation into the swizzled tiles.
+//   Warp 8:    one thread issues every tcgen05.mma (S(j+1) ahead of PV(j)) and commits
+//              their completion to mbarriers.
+// Every mbarrier wait is bounded; on a timeout the CTA flags KVQ_STATUS_TIMEOUT, stops, waits
+// (bounded) for its copies and MMAs in flight, and still releases its TMEM.
+#include "kvq_internal.cuh"
+#include "attn_args.cuh"
+
+namespace kvq {
+
+constexpr int PT_ROWS = 128;
+constexpr int PT_THREADS = 9 * 32;
+constexpr int PT_STAGE = 2 * HQ2B_BLOCK;  // compressed K + V block of one page (one layer/head)
+constexpr int SM_K = 0;                   // 2 x 32 KB
+constexpr int SM_V = 65536;               // 2 x 32 KB
+constexpr int SM_STG = 131072;            // 2 x 9,216 B
+constexpr int SM_BAR = SM_STG + 2 * PT_STAGE;
+constexpr int NUM_BARS = 17;
+constexpr int SM_ABORT = SM_BAR + NUM_BARS * 8;
+constexpr int SM_TMEM = SM_ABORT + 4;
+constexpr int PT_SMEM = SM_TMEM + 12 + 1024;  // + slack to align the base to 1,024 B
+constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
+constexpr int PT_SPIN = 1 << 16;
+constexpr float RESCALE_LOG2 = 8.0f;
+
+enum {
+  B_STG_FULL = 0, B_STG_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_V_FULL = 8,
+  B_S_FULL = 10, B_P_FULL = 12, B_PV_DONE = 14, B_Q_READY = 16
+};
+
+__device__ __forceinline__ uint32_t sm_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < PT_SPIN; i++) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(1000u)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------------------- tcgen05 wrappers
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// D(tmem) (+)= A(tmem) . B(smem descriptor)^T
+__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+      "r"(a), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
+#define TC_LD32(taddr, r)                                                                                        \
+  asm volatile(                                                                                                  \
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"   \
+      "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"                                       \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),           \
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),     \
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),   \
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])    \
+      : "r"(taddr))
+
+#define TC_ST32(taddr, r)                                                                                        \
+  asm volatile(                                                                                                  \
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"    \
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),                       \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),         \
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), \
+      "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),            \
+      "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                                      \
+      : "memory")
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+// shared-memory matrix descriptor: 128B swizzle, K-major, 8-row groups 1,024 B apart
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+  d |= (uint64_t)1 << 46;             // descriptor version of the sm_100 family
+  d |= (uint64_t)2 << 61;             // 128-byte swizzle
+  return d;
+}
+
+// instruction descriptor: D f32, A f16, B f16, both K-major, M x N
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// byte offset of 16 B chunk `chunk` (0..7) of `row` in a 128B-swizzled region (1,024 B atoms)
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 x) { return *reinterpret_cast<uint32_t*>(&x); }
+__device__ __forceinline__ __half2 u2h(uint32_t x) { return *reinterpret_cast<__half2*>(&x); }
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------- kernel
+// grid (splits, ceil(max_n_q / QT), lanes * H); PT_THREADS threads; PT_SMEM dynamic smem
+__global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const CacheView& c = a.c;
+  const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
+  const int QT = PT_ROWS / G;
+  const int b = blockIdx.z / H, h = blockIdx.z % H, qt = blockIdx.y, s = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- rows and keys of this CTA (uniform: early exits happen before any barrier)
+  const int len = a.seq_len[b];
+  const int nq = a.n_q[b], qoff = a.q_offset[b], qpos0 = a.q_pos0[b];
+  if (len < 0 || len > c.max_pages * P || nq < 0 || nq > a.max_n_q || qoff < 0 || (int64_t)qoff + nq > a.n_q_rows ||
+      qpos0 < 0 || (int64_t)qpos0 + nq > len) {
+    if (threadIdx.x == 0 && s == 0 && qt == 0 && h == 0) flag(c.status, KVQ_STATUS_BAD_LEN);
+    return;
+  }
+  const int q_first = qt * QT;
+  if (q_first >= nq) return;
+  const int q_last = min(nq, q_first + QT) - 1;
+  const int kmax = qpos0 + q_last + 1;
+  const int k0 = s * a.split_tokens;
+  if (k0 >= kmax) return;
+  const int k1 = min(k0 + a.split_tokens, kmax);
+  const int p0 = k0 / P;
+  const int ntiles = (k1 + P - 1) / P - p0;
+  const int ef = exact_from(len, c.window);
+
+  uint8_t* smem = smem_raw + ((1024u - (sm_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
+  auto BAR = [&](int i) { return sm_u32(&bars[i]); };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; i++) {
+      bar_init(BAR(B_STG_FULL + i), 1);
+      bar_init(BAR(B_STG_EMPTY + i), 4);
+      bar_init(BAR(B_K_FULL + i), 4);
+      bar_init(BAR(B_K_EMPTY + i), 1);
+      bar_init(BAR(B_V_FULL + i), 4);
+      bar_init(BAR(B_S_FULL + i), 1);
+      bar_init(BAR(B_P_FULL + i), 4);
+      bar_init(BAR(B_PV_DONE + i), 1);
+    }
+    bar_init(BAR(B_Q_READY), 4);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(sm_u32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool timed_out = false;
+
+  if (warp < 4) {
+    // =============================================================== softmax warps
+    const int row = 32 * warp + lane;
+    const int qi = row / G, g = row - (row / G) * G;
+    const bool row_valid = row < QT * G && q_first + qi < nq;
+    const int qpos = qpos0 + q_first + qi;
+    const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    // Q row -> TMEM columns [0,128) as fp16 pairs
+    for (int ch = 0; ch < 4; ch++) {
+      uint32_t r[32];
+      if (row_valid) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(a.q + ((int64_t)(qoff + q_first + qi) * Hq + h * G + g) * D + 64 * ch);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          const uint4 w = src[i];
+          r[4 * i + 0] = h2u(__floats2half2_rn(bf16_lo(w.x), bf16_hi(w.x)));
+          r[4 * i + 1] = h2u(__floats2half2_rn(bf16_lo(w.y), bf16_hi(w.y)));
+          r[4 * i + 2] = h2u(__floats2half2_rn(bf16_lo(w.z), bf16_hi(w.z)));
+          r[4 * i + 3] = h2u(__floats2half2_rn(bf16_lo(w.w), bf16_hi(w.w)));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) r[i] = 0u;
+      }
+      TC_ST32(tl + TM_Q + 32 * ch, r);
+    }
+    tc_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) bar_arrive(BAR(B_Q_READY));
+
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < ntiles; j++) {
+      const int buf = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) { timed_out = true; break; }
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_S_FULL + buf), par))) { timed_out = true; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      TC_LD32(tl + TM_S0 + 64 * buf, sv);
+      TC_LD32(tl + TM_S0 + 64 * buf + 32, (sv + 32));
+      tc_wait_ld();
+      const int key0 = (p0 + j) * P;
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int cidx = 0; cidx < 64; cidx++) {
+        const bool ok = row_valid && key0 + cidx <= qpos;
+        const float x = ok ? __uint_as_float(sv[cidx]) * a.scale_log2 : -INFINITY;
+        sv[cidx] = __float_as_uint(x);
+        tmax = fmaxf(tmax, x);
+      }
+      const float m_new = fmaxf(m_run, tmax);
+      const bool first = (j == 0) || (m_run == -INFINITY);
+      const bool need = !first && (m_new > m_run + RESCALE_LOG2);
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        // O must be stable: PV(j-1) complete
+        if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_PV_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1))) {
+          timed_out = true;
+          break;
+        }
+        tc_fence_after();
+        const float alpha = need ? exp2f(m_run - m_new) : 1.0f;
+        for (int ch = 0; ch < 8; ch++) {
+          uint32_t o[32];
+          TC_LD32(tl + TM_O + 32 * ch, o);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          TC_ST32(tl + TM_O + 32 * ch, o);
+        }
+        tc_wait_st();
+        if (need) {
+          l_run *= alpha;
+          m_run = m_new;
+        }
+      }
+      if (first) m_run = m_new;
+      const float m_use = m_run == -INFINITY ? 0.f : m_run;
+      uint32_t pr[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
+        const float e0 = x0 == -INFINITY ? 0.f : exp2f(x0 - m_use);
+        const float e1 = x1 == -INFINITY ? 0.f : exp2f(x1 - m_use);
+        psum += e0 + e1;
+        pr[i] = h2u(__floats2half2_rn(e0, e1));
+      }
+      l_run += psum;
+      TC_ST32(tl + TM_S0 + 64 * buf, pr);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(BAR(B_P_FULL + buf));
+    }
+    // ---- epilogue: (m, l, O) of this split
+    if (!timed_out && ntiles > 0) {
+      const int jl = ntiles - 1;
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_PV_DONE + (jl & 1)), (jl >> 1) & 1))) timed_out = true;
+    }
+    if (!timed_out) {
+      tc_fence_after();
+      const int64_t pidx = ((int64_t)(qoff + q_first + qi) * Hq + h * G + g) * a.max_splits + s;
+      for (int ch = 0; ch < 8; ch++) {
+        uint32_t o[32];
+        TC_LD32(tl + TM_O + 32 * ch, o);
+        tc_wait_ld();
+        if (row_valid) {
+          float4* dst = reinterpret_cast<float4*>(a.ws_o + pidx * D + 32 * ch);
+#pragma unroll
+          for (int i = 0; i < 8; i++)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+        }
+      }
+      if (row_valid) reinterpret_cast<float2*>(a.ws_ml)[pidx] = make_float2(m_run, l_run);
+    }
+  } else if (warp < 8) {
+    // =============================================================== TMA + dequant warps
+    const int tid = threadIdx.x - 128;
+    const int64_t lane_row = (int64_t)b * c.max_pages;
+    auto issue = [&](int j) -> bool {
+      const int buf = j & 1;
+      if (!bar_wait(BAR(B_STG_EMPTY + buf), ((j >> 1) & 1) ^ 1)) return false;
+      const int32_t phys = c.page_table[lane_row + p0 + j];
+      if (phys < 0 || phys >= c.pool_pages) {
+        flag(c.status, KVQ_STATUS_PAGE_OOB);
+        bar_arrive(BAR(B_STG_FULL + buf));
+        return true;
+      }
+      const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
+      const uint32_t dst = sm_u32(smem + SM_STG + buf * PT_STAGE);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(BAR(B_STG_FULL + buf)),
+                   "r"((uint32_t)PT_STAGE)
+                   : "memory");
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+          "l"(src), "r"((uint32_t)PT_STAGE), "r"(BAR(B_STG_FULL + buf))
+          : "memory");
+      return true;
+    };
+    int issued = 0;
+    if (tid == 0) {
+      for (; issued < 2 && issued < ntiles; issued++)
+        if (!issue(issued)) { timed_out = true; break; }
+    }
+    const __half2 two = __float2half2_rn(2.0f), m11 = __float2half2_rn(-11.0f);
+    for (int j = 0; j < ntiles && !timed_out; j++) {
+      const int buf = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) { timed_out = true; break; }
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_STG_FULL + buf), par))) { timed_out = true; break; }
+      const uint8_t* stg = smem + SM_STG + buf * PT_STAGE;
+      const int key0 = (p0 + j) * P;
+      // ---- K tile (B of S): element (key t, dim d) at atom d/64, row t, chunk (d%64)/8
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_K_EMPTY + buf), par ^ 1))) { timed_out = true; break; }
+      const uint32_t kb = sm_u32(smem + SM_K + buf * 32768);
+#pragma unroll 4
+      for (int i = 0; i < 16; i++) {
+        const int item = tid + 128 * i;
+        const int t = item >> 5, cc = item & 31;
+        const int kp = key0 + t;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (kp < len) {
+          if (kp >= ef) {
+            const uint4 w =
+                reinterpret_cast<const uint4*>(c.ring + ((((int64_t)b * c.num_layers + c.layer) * H + h) * P + (kp % P)) * D)[cc];
+            o.x = h2u(__floats2half2_rn(bf16_lo(w.x), bf16_hi(w.x)));
+            o.y = h2u(__floats2half2_rn(bf16_lo(w.y), bf16_hi(w.y)));
+            o.z = h2u(__floats2half2_rn(bf16_lo(w.z), bf16_hi(w.z)));
+            o.w = h2u(__floats2half2_rn(bf16_lo(w.w), bf16_hi(w.w)));
+          } else {
+            const uint32_t w16 = *reinterpret_cast<const uint16_t*>(stg + t * HQ2B_ROW + 2 * cc);
+            const uint4 sc = *reinterpret_cast<const uint4*>(stg + HQ2B_META_OFF + 16 * cc);
+            const uint32_t u = (w16 << 8) | (w16 << 22);
+            const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
+            uint32_t res[4];
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+              const uint32_t x = ((u >> (4 * p)) & 0x03000300u) | 0x44004400u;   // (4 + c) pairs
+              const __half2 y = __hfma2(u2h(x), two, m11);                        // 2c - 3, exact
+              res[p] = h2u(__hmul2(y, u2h(scs[p])));                              // s_d (2c - 3)
+            }
+            o = make_uint4(res[0], res[1], res[2], res[3]);
+          }
+        }
+        st_shared_v4(kb + (cc >> 3) * 8192 + swz(t, cc & 7), o);
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      __syncwarp();
+      if (lane == 0) bar_arrive(BAR(B_K_FULL + buf));
+      // ---- V^T tile (B of PV): element (dim d, key t) at row d, chunk t/8
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_PV_DONE + buf), par ^ 1))) { timed_out = true; break; }
+      const uint32_t vb = sm_u32(smem + SM_V + buf * 32768);
+      const uint8_t* vst = stg + HQ2B_BLOCK;
+#pragma unroll 1
+      for (int i = 0; i < 4; i++) {
+        const int item = tid + 128 * i;   // 512 items: byte column q x key chunk kc
+        const int q = item & 63, kc = item >> 6;
+        const int hf = q >> 5;
+        float v[4][8];
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+          const int t = 8 * kc + e;
+          const uint32_t byte = vst[t * HQ2B_ROW + q];
+          const uint32_t meta = *reinterpret_cast<const uint32_t*>(vst + HQ2B_META_OFF + t * 8 + 4 * hf);
+          const float sv = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
+          const float zv = half_bits_to_float((uint16_t)(meta >> 16));
+          const bool ok = key0 + t < len;
+#pragma unroll
+          for (int k = 0; k < 4; k++) v[k][e] = ok ? fmaf((float)((byte >> (2 * k)) & 3u), sv, zv) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const uint4 o = make_uint4(h2u(__floats2half2_rn(v[k][0], v[k][1])), h2u(__floats2half2_rn(v[k][2], v[k][3])),
+                                     h2u(__floats2half2_rn(v[k][4], v[k][5])), h2u(__floats2half2_rn(v[k][6], v[k][7])));
+          st_shared_v4(vb + swz(4 * q + k, kc), o);
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        bar_arrive(BAR(B_V_FULL + buf));
+        bar_arrive(BAR(B_STG_EMPTY + buf));
+      }
+      if (tid == 0 && issued < ntiles) {
+        if (!issue(issued)) timed_out = true;
+        issued++;
+      }
+      timed_out = __shfl_sync(0xFFFFFFFFu, timed_out, 0);
+    }
+    // copies still in flight must land before the CTA exits
+    if (tid == 0) {
+      for (int j = max(0, issued - 2); j < issued; j++) bar_wait(BAR(B_STG_FULL + (j & 1)), (j >> 1) & 1);
+    }
+  } else {
+    // =============================================================== MMA warp (one thread)
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(128, 64);
+      constexpr uint32_t IDESC_PV = idesc_f16(128, 256);
+      bool ok = bar_wait(BAR(B_Q_READY), 0);
+      tc_fence_after();
+      auto issue_s = [&](int j) -> bool {
+        const int buf = j & 1;
+        if (!bar_wait(BAR(B_K_FULL + buf), (j >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kb = sm_u32(smem + SM_K + buf * 32768);
+#pragma unroll
+        for (int ks = 0; ks < 16; ks++)
+          tc_mma_ts(tmem + TM_S0 + 64 * buf, tmem + TM_Q + 8 * ks, sw128_desc(kb + (ks >> 2) * 8192 + (ks & 3) * 32),
+                    IDESC_S, ks > 0);
+        tc_commit(BAR(B_S_FULL + buf));
+        tc_commit(BAR(B_K_EMPTY + buf));
+        return true;
+      };
+      int last_pv = -1;
+      if (ok && ntiles > 0) ok = issue_s(0);
+      for (int j = 0; j < ntiles && ok; j++) {
+        if (*abort_flag) { ok = false; break; }
+        if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
+        const int buf = j & 1;
+        const uint32_t par = (j >> 1) & 1;
+        if (!bar_wait(BAR(B_P_FULL + buf), par) || !bar_wait(BAR(B_V_FULL + buf), par)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vb = sm_u32(smem + SM_V + buf * 32768);
+#pragma unroll
+        for (int ks = 0; ks < 4; ks++)
+          tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_desc(vb + 32 * ks), IDESC_PV,
+                    (j > 0 || ks > 0) ? 1u : 0u);
+        tc_commit(BAR(B_PV_DONE + buf));
+        last_pv = j;
+      }
+      if (!ok) {
+        timed_out = true;
+        *abort_flag = 1;
+      }
+      // the MMAs issued must finish before TMEM is released
+      if (last_pv >= 0) bar_wait(BAR(B_PV_DONE + (last_pv & 1)), (last_pv >> 1) & 1);
+    }
+    __syncwarp();
+  }
+  if (timed_out) {
+    *abort_flag = 1;
+    if (lane == 0) flag(c.status, KVQ_STATUS_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem));
+  }
+}
+
+int launch_prefill_hq2b_tc(const AttnArgs& a, cudaStream_t stream) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!attr_set[dev]) {
+    cudaFuncSetAttribute(prefill_hq2b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, PT_SMEM);
+    attr_set[dev] = true;
+  }
+  const int QT = PT_ROWS / a.c.group;
+  dim3 grid(a.max_splits, (a.max_n_q + QT - 1) / QT, a.lanes * a.c.num_kv_heads);
+  prefill_hq2b_tc<<<grid, PT_THREADS, PT_SMEM, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+}  // namespace kvq

@@ -329,6 +329,20 @@ class Workload:
         return x
 
 
+def kv_np_parallel(wl: "Workload", layer: int, lane: int, pos0: int, n: int, kv: int, chunk: int = 4096,
+                   threads: Optional[int] = None) -> np.ndarray:
+    """``wl.kv_np`` computed in parallel chunks of tokens (numpy releases the GIL)."""
+    import concurrent.futures as cf
+    import os
+    if n <= chunk:
+        return wl.kv_np(layer, lane, pos0, n, kv)
+    threads = threads or max(1, min(32, os.cpu_count() or 1))
+    starts = list(range(pos0, pos0 + n, chunk))
+    with cf.ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(lambda p: wl.kv_np(layer, lane, p, min(chunk, pos0 + n - p), kv), starts))
+    return np.concatenate(parts, 0)
+
+
 def _table(lanes_pages: List[np.ndarray], max_pages: int) -> np.ndarray:
     t = np.full((len(lanes_pages), max_pages), -1, dtype=np.int32)
     for b, p in enumerate(lanes_pages):

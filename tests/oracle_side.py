@@ -26,14 +26,9 @@ def assert_close(gpu, ref, atol=ATOL, rtol=RTOL, what=""):
     return float(err.max())
 
 
-def host_kv(wl: synth.Workload, layer: int, lane: int, pos0: int, n: int, kv: int, chunk: int = 4096):
-    """bf16 bits [n][H][256], generated in parallel chunks (numpy releases the GIL)."""
-    if n <= chunk:
-        return wl.kv_np(layer, lane, pos0, n, kv)
-    starts = list(range(pos0, pos0 + n, chunk))
-    with cf.ThreadPoolExecutor(THREADS) as ex:
-        parts = list(ex.map(lambda p: wl.kv_np(layer, lane, p, min(chunk, pos0 + n - p), kv), starts))
-    return np.concatenate(parts, 0)
+def host_kv(wl: synth.Workload, layer: int, lane: int, pos0: int, n: int, kv: int):
+    """bf16 bits [n][H][256] regenerated on the host (parallel chunks)."""
+    return synth.kv_np_parallel(wl, layer, lane, pos0, n, kv, threads=THREADS)
 
 
 class LaneCache:
