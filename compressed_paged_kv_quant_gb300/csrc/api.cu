@@ -131,6 +131,7 @@ const char* kvq_strerror(int code) {
     case KVQ_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case KVQ_ERR_CUDA: return "CUDA launch error";
     case KVQ_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
+    case KVQ_ERR_SCRATCH_LIMIT: return "request exceeds the static scratch of paged_decode_attn_noalloc";
     default: return "unknown error";
   }
 }

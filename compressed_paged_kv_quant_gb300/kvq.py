@@ -23,6 +23,8 @@ ERR_UNSUPPORTED = -2
 ERR_WORKSPACE_TOO_SMALL = -3
 ERR_CUDA = -4
 ERR_ALIGNMENT = -5
+ERR_SCRATCH_LIMIT = -6
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 STATUS_PAGE_OOB = 1
 STATUS_LEN_GT_TABLE = 2
@@ -32,7 +34,8 @@ STATUS_TIMEOUT = 16
 
 EXPORTS = ("kvq_page_bytes", "kvq_token_bytes", "kvq_ring_bytes", "kvq_pool_pages",
            "kvq_decode_workspace_bytes", "kvq_prefill_workspace_bytes", "kvq_strerror",
-           "kvq_build_arch", "kv_quant_append", "paged_decode_attn", "paged_prefill_attn")
+           "kvq_build_arch", "kv_quant_append", "paged_decode_attn", "paged_prefill_attn",
+           "paged_decode_attn_noalloc")
 
 
 class KvqError(RuntimeError):
@@ -95,6 +98,8 @@ def lib():
             L.paged_prefill_attn.argtypes = [G, i32, P, sz, P, i32, P, i32, i32, P, P, P, i32, i32, P, i32,
                                              P, f32, P, sz, P, P, P]
             L.paged_prefill_attn.restype = i32
+            L.paged_decode_attn_noalloc.argtypes = [G, i32, P, sz, P, i32, P, i32, i32, P, i32, P, f32, P, P, P]
+            L.paged_decode_attn_noalloc.restype = i32
             _lib = L
     return _lib
 
@@ -175,6 +180,18 @@ def paged_decode_attn(g: Geom, layer: int, pool, ring, window: int, page_table, 
                                  max_seq_len, _ptr(q), float(sm_scale), _ptr(workspace),
                                  _nbytes(workspace), _ptr(out), _ptr(status), _stream(stream))
     _check(rc, "paged_decode_attn")
+
+
+def paged_decode_attn_noalloc(g: Geom, layer: int, pool, ring, window: int, page_table, seq_len,
+                              max_seq_len: int, q, sm_scale: float, out, status, stream=None,
+                              lanes: Optional[int] = None):
+    """paged_decode_attn with the library's static scratch instead of a caller workspace, for
+    callers that cannot allocate device memory (see ``paged_decode_attn_noalloc`` in kvq.h)."""
+    n_lanes = page_table.shape[0] if lanes is None else lanes
+    rc = lib().paged_decode_attn_noalloc(ctypes.byref(g), layer, _ptr(pool), _nbytes(pool), _ptr(ring), window,
+                                         _ptr(page_table), page_table.shape[1], n_lanes, _ptr(seq_len), max_seq_len,
+                                         _ptr(q), float(sm_scale), _ptr(out), _ptr(status), _stream(stream))
+    _check(rc, "paged_decode_attn_noalloc")
 
 
 def paged_prefill_attn(g: Geom, layer: int, pool, ring, window: int, page_table, q_pos0, n_q,

@@ -60,6 +60,7 @@ typedef struct {
 #define KVQ_ERR_WORKSPACE_TOO_SMALL (-3)
 #define KVQ_ERR_CUDA (-4)
 #define KVQ_ERR_ALIGNMENT (-5)
+#define KVQ_ERR_SCRATCH_LIMIT (-6) /* paged_decode_attn_noalloc: request exceeds its static scratch */
 
 /* device status bits OR-ed into *d_status */
 #define KVQ_STATUS_PAGE_OOB 1      /* a page-table entry the call needed is outside [0, pool pages) */
@@ -174,6 +175,30 @@ int paged_prefill_attn(const kvq_geom* geom, int layer, const void* pool, size_t
                        const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale,
                        void* workspace, size_t ws_bytes, float* out, int32_t* d_status,
                        kvq_stream_t stream);
+
+/*
+ * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.  The pages have
+ * no counterpart of this call: it exists for callers that cannot allocate device memory --
+ * code running inside a CUDA graph capture it does not own, plugins of an engine whose
+ * allocator owns all of the GPU's memory, hosts that forbid allocation after start-up.
+ *   Same arguments, results and errors as paged_decode_attn, minus `workspace`/`ws_bytes`:
+ *   the split partials live in one static device array of KVQ_NOALLOC_SCRATCH_BYTES
+ *   (32 MiB) inside the library, which every GPU that loads the library keeps until the
+ *   process exits.  The call allocates nothing and calls no allocating routine.
+ *   Limit: kvq_decode_workspace_bytes(geom, lanes, max_seq_len) must not exceed
+ *   KVQ_NOALLOC_SCRATCH_BYTES, else KVQ_ERR_SCRATCH_LIMIT and nothing is launched (at the
+ *   27B geometry that is room for 8 lanes x 40,960 tokens several times over).
+ *   The first call on a device looks up the array's device address (once per device, with
+ *   that device current); make that first call before any stream capture.
+ *   Every call shares the array: calls whose kernels may overlap on the GPU (different
+ *   streams without ordering) race on it.  Nothing in it needs clearing -- each call writes
+ *   every partial it reads.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (32u << 20)
+int paged_decode_attn_noalloc(const kvq_geom* geom, int layer, const void* pool, size_t pool_bytes,
+                              const void* ring, int window, const int32_t* page_table, int max_pages,
+                              int lanes, const int32_t* seq_len, int max_seq_len, const void* q,
+                              float sm_scale, float* out, int32_t* d_status, kvq_stream_t stream);
 
 #ifdef __cplusplus
 }
