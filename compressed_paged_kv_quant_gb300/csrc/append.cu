@@ -54,8 +54,11 @@ __device__ __forceinline__ bool row8_ok(uint4 w) {
   return ok;
 }
 
-// Page-close quantization of K, per channel over the page's 64 keys.
-__global__ void __launch_bounds__(256) append_kclose_kernel(AppendArgs a) {
+// Page-close quantization of K, per channel over the page's 64 keys.  512 threads: thread
+// (part, d) handles channel d = tid % 256 for keys 32*part .. 32*part + 31.
+constexpr int KCLOSE_THREADS = 512;
+
+__global__ void __launch_bounds__(KCLOSE_THREADS) append_kclose_kernel(AppendArgs a) {
   const int b = blockIdx.z, h = blockIdx.y;
   int start, n, off;
   if (!read_lane(a, b, start, n, off)) return;
@@ -72,32 +75,38 @@ __global__ void __launch_bounds__(256) append_kclose_kernel(AppendArgs a) {
     if (threadIdx.x == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
     return;
   }
-  const int d = threadIdx.x;
+  const int d = threadIdx.x & (D - 1), part = threadIdx.x >> 8;
   const int H = c.num_kv_heads;
-  float x[P];
+  constexpr int T = P / 2;
+  float x[T];
   float amax = 0.0f;
   bool bad = false;
 #pragma unroll
-  for (int t = 0; t < P; t++) {
+  for (int i = 0; i < T; i++) {
+    const int t = T * part + i;
     const int pos = p * P + t;
     __nv_bfloat16 e = pos < start ? a.ring[ring_row_offset(c, b, h, t) + d]
                                   : a.k[((int64_t)(off + pos - start) * H + h) * D + d];
-    x[t] = __bfloat162float(e);
-    bad |= !finite16(x[t]);
-    amax = fmaxf(amax, fabsf(x[t]));
+    x[i] = __bfloat162float(e);
+    bad |= !finite16(x[i]);
+    amax = fmaxf(amax, fabsf(x[i]));
   }
+  __shared__ float part_max[2][D];
+  __shared__ __align__(16) uint8_t codes[P * HQ2B_ROW];
+  part_max[part][d] = amax;
   if (__syncthreads_or(bad)) {
-    if (d == 0) flag(c.status, KVQ_STATUS_BAD_INPUT);
+    if (threadIdx.x == 0) flag(c.status, KVQ_STATUS_BAD_INPUT);
     return;
   }
+  amax = fmaxf(part_max[0][d], part_max[1][d]);
   const __half sh = __float2half_rn(__fdiv_rn(amax, 3.0f));
   const float sf = __half2float(sh);
-  __shared__ __align__(16) uint8_t codes[P * HQ2B_ROW];
 #pragma unroll
-  for (int t = 0; t < P; t++) {
+  for (int i = 0; i < T; i++) {
+    const int t = T * part + i;
     int code = 2;
     if (sf != 0.0f) {
-      float u = __fdiv_rn(x[t], sf);
+      float u = __fdiv_rn(x[i], sf);
       u = __fadd_rn(u, 3.0f);
       u = __fmul_rn(0.5f, u);
       u = fminf(fmaxf(rintf(u), 0.0f), 3.0f);
@@ -109,9 +118,11 @@ __global__ void __launch_bounds__(256) append_kclose_kernel(AppendArgs a) {
     if ((d & 3) == 0) codes[t * HQ2B_ROW + d / 4] = (uint8_t)bits;
   }
   __syncthreads();
-  uint8_t* kblk = a.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
-  reinterpret_cast<uint4*>(kblk)[threadIdx.x] = reinterpret_cast<const uint4*>(codes)[threadIdx.x];
-  reinterpret_cast<__half*>(kblk + HQ2B_META_OFF)[d] = sh;
+  if (threadIdx.x < D) {
+    uint8_t* kblk = a.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
+    reinterpret_cast<uint4*>(kblk)[threadIdx.x] = reinterpret_cast<const uint4*>(codes)[threadIdx.x];
+    reinterpret_cast<__half*>(kblk + HQ2B_META_OFF)[d] = sh;
+  }
 }
 
 // One warp per (token, head): V row quantization (HQ2B) or plain stores (BF16), plus the ring.
@@ -200,7 +211,7 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
   AppendArgs a{c, pool, ring, start_pos, n_new, tok_offset, max_new, n_rows, lanes, k, v};
   if (fmt == KVQ_FMT_HQ2B) {
     dim3 gk(max_new / P + 1, c.num_kv_heads, lanes);
-    append_kclose_kernel<<<gk, 256, 0, stream>>>(a);
+    append_kclose_kernel<<<gk, KCLOSE_THREADS, 0, stream>>>(a);
     dim3 gr((max_new + ROWS_PER_CTA - 1) / ROWS_PER_CTA, lanes);
     append_rows_kernel<KVQ_FMT_HQ2B><<<gr, 256, 0, stream>>>(a);
   } else {

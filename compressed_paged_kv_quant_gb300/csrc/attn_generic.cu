@@ -159,8 +159,10 @@ __global__ void __launch_bounds__(256) attn_combine(AttnArgs a, int decode, int 
   const int64_t p0 = ((int64_t)row * Hq + j) * a.max_splits;
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + p0;
   float mx = -INFINITY;
+#pragma unroll 8
   for (int s = 0; s < nsplit; s++) mx = fmaxf(mx, ml[s].x);
   float den = 0.0f, num = 0.0f;
+#pragma unroll 8
   for (int s = 0; s < nsplit; s++) {
     const float2 e = ml[s];
     const float w = e.x == -INFINITY ? 0.0f : exp2f(e.x - mx);

@@ -34,14 +34,19 @@
 namespace kvq {
 
 constexpr int DEC_WARPS = 4;
-constexpr int DEC_CTAS_PER_SM = 2;
-constexpr int DEC_STAGES = 2;
+#ifndef KVQ_DEC_CTAS_PER_SM
+#define KVQ_DEC_CTAS_PER_SM 2
+#endif
+#ifndef KVQ_DEC_STAGES
+#define KVQ_DEC_STAGES 2
+#endif
+constexpr int DEC_CTAS_PER_SM = KVQ_DEC_CTAS_PER_SM;  // resident CTAs per SM the grid is sized for
+constexpr int DEC_STAGES = KVQ_DEC_STAGES;            // pages in flight per warp
 constexpr int STAGE_BYTES = 2 * HQ2B_BLOCK;  // K block + V block of one page, one layer/head
 constexpr int V_OFF = HQ2B_BLOCK;
 constexpr int MIN_PAGES_PER_WARP = 2;
-constexpr int DEC_MAX_SLOTS = 48;            // partial records per (lane, query head), at most
+constexpr int DEC_MAX_SLOTS = 96;            // partial records per (lane, query head), at most
 constexpr int SPIN_LIMIT = 1 << 16;          // bounded mbarrier waits (x ~1 us hint)
-constexpr uint32_t ONES_H2 = 0x3C003C00u;    // fp16x2 (1, 1)
 
 // pages of lane b handled by the MMA path (everything before its exact tail)
 __device__ __forceinline__ int main_pages(const CacheView& c, const int32_t* seq_len, int b, bool* bad = nullptr) {
@@ -87,8 +92,36 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// codes at bits 8-9 and 24-25 -> fp16x2 (4 + c_lo, 4 + c_hi)
-__device__ __forceinline__ uint32_t code_pair(uint32_t x) { return (x & 0x03000300u) | 0x44004400u; }
+// A-operand pairs straight from a code word.  x << 2 brings codes 0..3 of the low byte of each
+// 16-bit half to mantissa bits 2-3, 4-5, 6-7, 8-9; x >> 6 does the same for the high byte.
+// OR-ing in the exponent of 256, 64, 16 or 4 makes each half read exactly M + c; one HFMA2
+// (on the FMA pipe) then yields 2c - 3 (keys) or c (values) exactly.
+__device__ __forceinline__ uint32_t code_raw(uint32_t x, int pos) {
+  const uint32_t mask = pos == 0 ? 0x000C000Cu : pos == 1 ? 0x00300030u : pos == 2 ? 0x00C000C0u : 0x03000300u;
+  const uint32_t magic = pos == 0 ? 0x5C005C00u : pos == 1 ? 0x54005400u : pos == 2 ? 0x4C004C00u : 0x44004400u;
+  return (x & mask) | magic;
+}
+__device__ __forceinline__ uint32_t h2fma(uint32_t a, uint32_t b, uint32_t c) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b), *reinterpret_cast<__half2*>(&c));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+// key code as 2c - 3: (M + c) * 2 - (2M + 3)
+__device__ __forceinline__ uint32_t code_k(uint32_t x, int pos) {
+  const uint32_t neg = pos == 0 ? 0xE006E006u : pos == 1 ? 0xD818D818u : pos == 2 ? 0xD060D060u : 0xC980C980u;
+  return h2fma(code_raw(x, pos), 0x40004000u, neg);
+}
+// value code as c: (M + c) * 1 - M
+__device__ __forceinline__ uint32_t code_v(uint32_t x, int pos) {
+  const uint32_t neg = pos == 0 ? 0xDC00DC00u : pos == 1 ? 0xD400D400u : pos == 2 ? 0xCC00CC00u : 0xC400C400u;
+  return h2fma(code_raw(x, pos), 0x3C003C00u, neg);
+}
+
+// 2^x for the softmax (x <= 0 or -inf); one MUFU.EX2, relative error ~2^-22
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -224,20 +257,15 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
 
   // per-thread state: heads e0 = 2*cq, e1 = 2*cq + 1 of the group
   float O[16][4];
-  float Vc[2][4];
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, Z00 = 0.f, Z01 = 0.f, Z10 = 0.f, Z11 = 0.f;
   uint32_t qh[16][2];
-  const float sc2 = 2.0f * a.scale_log2, csc = -11.0f * a.scale_log2;
+  const float sl2 = a.scale_log2;
 
   auto reset = [&]() {
 #pragma unroll
     for (int i = 0; i < 16; i++)
 #pragma unroll
       for (int e = 0; e < 4; e++) O[i][e] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 2; i++)
-#pragma unroll
-      for (int e = 0; e < 4; e++) Vc[i][e] = 0.f;
     m0 = m1 = -INFINITY;
     l0 = l1 = Z00 = Z01 = Z10 = Z11 = 0.f;
   };
@@ -290,8 +318,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
           float v[16];
 #pragma unroll
           for (int i = 0; i < 8; i++) {
-            v[i] = O[8 * hf + i][e] - 4.0f * Vc[hf][e] + z;
-            v[8 + i] = O[8 * hf + i][2 + e] - 4.0f * Vc[hf][2 + e] + z;
+            v[i] = O[8 * hf + i][e] + z;
+            v[8 + i] = O[8 * hf + i][2 + e] + z;
           }
           float4* d4 = reinterpret_cast<float4*>(dst + 128 * hf + 16 * r);
 #pragma unroll
@@ -318,66 +346,49 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
       phase ^= 1u << slot;
       const uint8_t* st = ring_smem + slot * STAGE_BYTES;
 
-      // ---- q~ = q (.) s_page in the contraction order
-      uint32_t bq[16][2];
-      {
-        uint32_t sw[32];
-        const uint4* s4 = reinterpret_cast<const uint4*>(st + HQ2B_META_OFF + 128 * cq);
-#pragma unroll
-        for (int i = 0; i < 8; i++) {
-          const uint4 v = s4[i];
-          sw[4 * i] = v.x; sw[4 * i + 1] = v.y; sw[4 * i + 2] = v.z; sw[4 * i + 3] = v.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; j++)
-#pragma unroll
-          for (int i = 0; i < 4; i++) {
-            const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-            const uint32_t s01 = __byte_perm(sw[8 * j + (i >> 1)], sw[8 * j + 4 + (i >> 1)], sel);
-            const uint32_t s23 = __byte_perm(sw[8 * j + 2 + (i >> 1)], sw[8 * j + 6 + (i >> 1)], sel);
-            bq[4 * j + i][0] = h2mul(qh[4 * j + i][0], s01);
-            bq[4 * j + i][1] = h2mul(qh[4 * j + i][1], s23);
-          }
-      }
-      // ---- sum(q~) per head, and S^T for the four 16-token m-tiles
-      float cr[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---- S^T for the four 16-token m-tiles.  k-step ks = 4j + i of thread column cq covers
+      // dims 64cq + 16j + {i, i+8} (A regs 0/1: codes of bytes 0/2 of word j) and
+      // {i+4, i+12} (A regs 2/3: bytes 1/3); q~ = q (.) s_page is formed per word j from the
+      // natural-order scale pairs.
       float S[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; mt++)
 #pragma unroll
         for (int e = 0; e < 4; e++) S[mt][e] = 0.f;
-      uint32_t wa[4][4], wb[4][4];
-#pragma unroll
-      for (int mt = 0; mt < 4; mt++) {
-        const uint4 ka = *reinterpret_cast<const uint4*>(st + (16 * mt + perm_row(r)) * HQ2B_ROW + 16 * cq);
-        const uint4 kb = *reinterpret_cast<const uint4*>(st + (16 * mt + 8 + perm_row(r)) * HQ2B_ROW + 16 * cq);
-        wa[mt][0] = ka.x; wa[mt][1] = ka.y; wa[mt][2] = ka.z; wa[mt][3] = ka.w;
-        wb[mt][0] = kb.x; wb[mt][1] = kb.y; wb[mt][2] = kb.z; wb[mt][3] = kb.w;
-      }
-      // k-step outer, m-tile inner: five independent accumulator chains interleave
+      const uint8_t* krow_a = st + perm_row(r) * HQ2B_ROW + 16 * cq;
+      const uint8_t* krow_b = st + (8 + perm_row(r)) * HQ2B_ROW + 16 * cq;
+      const uint8_t* kscale = st + HQ2B_META_OFF + 128 * cq;
 #pragma unroll
       for (int j = 0; j < 4; j++) {
+        const uint4 s_lo = *reinterpret_cast<const uint4*>(kscale + 32 * j);       // dims 16j .. 16j+7
+        const uint4 s_hi = *reinterpret_cast<const uint4*>(kscale + 32 * j + 16);  // dims 16j+8 .. 16j+15
+        const uint32_t slo[4] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w};
+        const uint32_t shi[4] = {s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+        uint32_t bq[4][2];
 #pragma unroll
         for (int i = 0; i < 4; i++) {
-          const uint32_t b0 = bq[4 * j + i][0], b1 = bq[4 * j + i][1];
+          const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+          bq[i][0] = h2mul(qh[4 * j + i][0], __byte_perm(slo[i >> 1], shi[i >> 1], sel));
+          bq[i][1] = h2mul(qh[4 * j + i][1], __byte_perm(slo[2 + (i >> 1)], shi[2 + (i >> 1)], sel));
+        }
 #pragma unroll
-          for (int mt = 0; mt < 4; mt++) {
-            const uint32_t ua = wa[mt][j] << 8, ub = wb[mt][j] << 8;
-            mma16816(S[mt], code_pair(ua >> (2 * i)), code_pair(ub >> (2 * i)), code_pair(wa[mt][j] >> (2 * i)),
-                     code_pair(wb[mt][j] >> (2 * i)), b0, b1);
-          }
-          mma16816(cr, ONES_H2, ONES_H2, ONES_H2, ONES_H2, b0, b1);
+        for (int mt = 0; mt < 4; mt++) {
+          const uint32_t wa = *reinterpret_cast<const uint32_t*>(krow_a + 16 * mt * HQ2B_ROW + 4 * j);
+          const uint32_t wb = *reinterpret_cast<const uint32_t*>(krow_b + 16 * mt * HQ2B_ROW + 4 * j);
+          const uint32_t la = wa << 2, ra = wa >> 6, lb = wb << 2, rb = wb >> 6;
+#pragma unroll
+          for (int i = 0; i < 4; i++)
+            mma16816(S[mt], code_k(la, i), code_k(lb, i), code_k(ra, i), code_k(rb, i), bq[i][0], bq[i][1]);
         }
       }
       // ---- online softmax (log2 domain)
-      const float cc0 = csc * cr[0], cc1 = csc * cr[1];
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < 4; mt++) {
-        S[mt][0] = fmaf(sc2, S[mt][0], cc0);
-        S[mt][1] = fmaf(sc2, S[mt][1], cc1);
-        S[mt][2] = fmaf(sc2, S[mt][2], cc0);
-        S[mt][3] = fmaf(sc2, S[mt][3], cc1);
+        S[mt][0] *= sl2;
+        S[mt][1] *= sl2;
+        S[mt][2] *= sl2;
+        S[mt][3] *= sl2;
         mx0 = fmaxf(mx0, fmaxf(S[mt][0], S[mt][2]));
         mx1 = fmaxf(mx1, fmaxf(S[mt][1], S[mt][3]));
       }
@@ -387,16 +398,16 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
       }
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
       m0 = mn0;
       m1 = mn1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int mt = 0; mt < 4; mt++) {
-        S[mt][0] = exp2f(S[mt][0] - mn0);
-        S[mt][1] = exp2f(S[mt][1] - mn1);
-        S[mt][2] = exp2f(S[mt][2] - mn0);
-        S[mt][3] = exp2f(S[mt][3] - mn1);
+        S[mt][0] = ex2(S[mt][0] - mn0);
+        S[mt][1] = ex2(S[mt][1] - mn1);
+        S[mt][2] = ex2(S[mt][2] - mn0);
+        S[mt][3] = ex2(S[mt][3] - mn1);
         ps0 += S[mt][0] + S[mt][2];
         ps1 += S[mt][1] + S[mt][3];
       }
@@ -407,10 +418,6 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
 #pragma unroll
         for (int i = 0; i < 16; i++) {
           O[i][0] *= al0; O[i][1] *= al1; O[i][2] *= al0; O[i][3] *= al1;
-        }
-#pragma unroll
-        for (int hf = 0; hf < 2; hf++) {
-          Vc[hf][0] *= al0; Vc[hf][1] *= al1; Vc[hf][2] *= al0; Vc[hf][3] *= al1;
         }
       }
       // ---- P (.) s_v per half, sum(P z), and the B fragments of P.V
@@ -434,7 +441,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
           Bv[1][mt][rr] = movmatrix_t(pack_h2(pa * s1, pb * s1));
         }
       }
-      // ---- O^T += V^ . P'^T
+      // ---- O^T += V^ . P'^T: a fp16 pair holds one dim of two tokens (bytes permuted so each
+      // half of a word is one token) as the exact code c
       const int t0 = perm_row(2 * cq), t1 = perm_row(2 * cq + 1);
 #pragma unroll
       for (int mt = 0; mt < 4; mt++) {
@@ -445,21 +453,22 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
           const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + t1) * HQ2B_ROW);
           const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t0) * HQ2B_ROW);
           const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t1) * HQ2B_ROW);
-          uint32_t x01[4], x23[4];
+          // [tok_a byte k, tok_a byte k+1, tok_b byte k, tok_b byte k+1], k = 0 (dims 16r..16r+7) or 2 (+8)
+          const uint32_t x[4] = {__byte_perm(w0, w1, 0x5410u), __byte_perm(w0, w1, 0x7632u),
+                                 __byte_perm(w2, w3, 0x5410u), __byte_perm(w2, w3, 0x7632u)};
+          uint32_t lo[4], hi[4];
 #pragma unroll
-          for (int bb = 0; bb < 4; bb++) {
-            const uint32_t sel = (uint32_t)(bb | (bb << 4) | ((4 + bb) << 8) | ((4 + bb) << 12));
-            x01[bb] = __byte_perm(w0, w1, sel);
-            x23[bb] = __byte_perm(w2, w3, sel);
+          for (int k = 0; k < 4; k++) {
+            lo[k] = x[k] << 2;  // codes of the first byte of each half
+            hi[k] = x[k] >> 6;  // codes of the second byte
           }
 #pragma unroll
           for (int i8 = 0; i8 < 8; i8++) {
-            const int blo = i8 >> 2, ci = i8 & 3;  // byte (0/1) for row r, code index
-            mma16816(O[8 * hf + i8], code_pair(x01[blo] >> (2 * ci)), code_pair(x01[blo + 2] >> (2 * ci)),
-                     code_pair(x23[blo] >> (2 * ci)), code_pair(x23[blo + 2] >> (2 * ci)), Bv[hf][mt][0],
-                     Bv[hf][mt][1]);
+            const int pos = i8 & 3;
+            const uint32_t* src = i8 < 4 ? lo : hi;
+            mma16816(O[8 * hf + i8], code_v(src[0], pos), code_v(src[1], pos), code_v(src[2], pos),
+                     code_v(src[3], pos), Bv[hf][mt][0], Bv[hf][mt][1]);
           }
-          mma16816(Vc[hf], ONES_H2, ONES_H2, ONES_H2, ONES_H2, Bv[hf][mt][0], Bv[hf][mt][1]);
         }
       }
       __syncwarp();
@@ -617,10 +626,12 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
   }
   const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + p0;
   float M = -INFINITY;
+#pragma unroll 8
   for (int k = 0; k < nk; k++) M = fmaxf(M, ml[k].x);
 #pragma unroll
   for (int w = 0; w < 8; w++) M = fmaxf(M, wm[w]);
   float num = 0.f, den = 0.f;
+#pragma unroll 8
   for (int k = 0; k < nk; k++) {
     const float2 e = ml[k];
     const float w = e.x == -INFINITY ? 0.f : exp2f(e.x - M);

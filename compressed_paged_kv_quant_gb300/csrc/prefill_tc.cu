@@ -373,12 +373,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
           } else {
             const uint32_t w16 = *reinterpret_cast<const uint16_t*>(stg + t * HQ2B_ROW + 2 * cc);
             const uint4 sc = *reinterpret_cast<const uint4*>(stg + HQ2B_META_OFF + 16 * cc);
-            const uint32_t u = (w16 << 8) | (w16 << 22);
+            // byte k of the code word holds dims 8cc + 4k .. +3; spread each byte so that codes
+            // (2p, 2p+1) of the chunk land in mantissa bits 8-9 of the two halves
+            const uint32_t lo = w16 & 0xFFu, hi = w16 >> 8;
+            const uint32_t ua = (lo << 8) | (lo << 22), ub = (hi << 8) | (hi << 22);
+            const uint32_t spread[4] = {ua, ua >> 4, ub, ub >> 4};
             const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
             uint32_t res[4];
 #pragma unroll
             for (int p = 0; p < 4; p++) {
-              const uint32_t x = ((u >> (4 * p)) & 0x03000300u) | 0x44004400u;   // (4 + c) pairs
+              const uint32_t x = (spread[p] & 0x03000300u) | 0x44004400u;        // (4 + c) pairs
               const __half2 y = __hfma2(u2h(x), two, m11);                        // 2c - 3, exact
               res[p] = h2u(__hmul2(y, u2h(scs[p])));                              // s_d (2c - 3)
             }

@@ -255,4 +255,7 @@ def test_flat_attention_over_131072_keys_keeps_full_mass():
     dw.decode(0, q, ws, out)
     o = out.cpu().numpy()
     ref, _ = oracle.decode(g, 0, pool, ring, 0, wl.page_table, 1, [n], np.zeros((1, 4, 256), np.uint16), 1.0)
-    assert_close(o, ref, atol=1e-5, rtol=1e-5, what="flat 131072")
+    # 2e-4 on unit-scale values: the FP32 partials lose nothing measurable (a bf16 running sum
+    # would be off by ~1.0); what remains is the tensor core's own FP32 accumulation within a
+    # warp's run of pages, well inside the 2e-3 + 1e-3 |ref| contract
+    assert_close(o, ref, atol=2e-4, rtol=2e-4, what="flat 131072")
