@@ -70,7 +70,7 @@ class Clocks:
                 ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
-                 "--format=csv,noheader,nounits", "-lms", "200", "-i", str(_device_index())],
+                 "--format=csv,noheader,nounits", "-lms", "50", "-i", str(_device_index())],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -272,18 +272,24 @@ def run_gpu(args):
     tokens_per_step = lanes * ctx
     value = world * tokens_per_step / (ms / 1000.0)
 
-    # per-call duration of the attention (CUDA events on the launching stream, same inputs)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
-    call_ms = []
+    # per-call duration of the attention: the L decode calls of one step captured alone in a
+    # graph (no host launch gaps), CUDA events on the launching stream around its replays
+    gd = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gd, stream=stream):
+        for l in range(L):
+            dw.decode(l, q_v[l], ws, step_out[l])
+    stream.synchronize()
     with torch.cuda.stream(stream):
-        for _ in range(max(3, args.steps)):
-            for l in range(L):
-                ev[l][0].record(stream)
-                dw.decode(l, q_v[l], ws, step_out[l])
-                ev[l][1].record(stream)
-            stream.synchronize()
-            call_ms += [x.elapsed_time(y) for x, y in ev]
-    call_ms = statistics.median(call_ms)
+        for _ in range(3):
+            gd.replay()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(3, args.steps)
+        d0.record(stream)
+        for _ in range(reps):
+            gd.replay()
+        d1.record(stream)
+    stream.synchronize()
+    call_ms = d0.elapsed_time(d1) / (reps * L)
     attn_bytes = lanes * ctx * H * 144          # compressed K+V bytes one layer's attention reads
     peak, peak_src = _peaks()
     achieved = attn_bytes / (call_ms / 1000.0) / 1e9
@@ -316,6 +322,8 @@ def run_gpu(args):
         e2e_ms = float(t.item())
     e2e_value = world * tokens_per_step / (e2e_ms / 1000.0)
 
+    prefill = None if args.no_prefill else run_prefill(args, dev, stream)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         od = OracleDecode(seed=args.seed)
@@ -335,18 +343,93 @@ def run_gpu(args):
                              "algorithmic_bytes_per_launch": attn_bytes},
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": 4 * L * args.steps,
-                "clocks": clk}
+                "gpu_launches": 3 * L * args.steps,
+                "clocks": clk,
+                "prefill": prefill}
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
     return 0
 
 
+def prefill_flops(prefix, chunk, q_heads):
+    """Causal attention FLOPs of one layer: 4 * 256 per (query, key) pair per query head."""
+    pairs = chunk * prefix + chunk * (chunk + 1) // 2
+    return 4.0 * 256 * pairs * q_heads
+
+
+def run_prefill(args, dev, stream):
+    """Chunked prefill over a compressed prefix (65,536 + 1,024 tokens, 16 layers): each layer
+    appends the chunk's K/V, then paged_prefill_attn with a garbage-filled workspace."""
+    import torch
+
+    from compressed_paged_kv_quant_gb300 import kvq, synth
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+    prefix, chunk = args.prefill_prefix, 1024
+    wl = synth.chunked_prefill_27b(prefix=prefix, chunk=chunk, layers=args.layers)
+    L = wl.num_layers
+    with torch.cuda.stream(stream):
+        dw = DeviceWorkload(wl, kvq.FMT_HQ2B, dev, fill=None, stream=stream.cuda_stream)
+        dw.fill_history([prefix], chunk=16384)
+        ks = [wl.kv_torch(l, 0, prefix, chunk, 0, dev) for l in range(L)]
+        vs = [wl.kv_torch(l, 0, prefix, chunk, 1, dev) for l in range(L)]
+        qs = [wl.q_torch(l, 0, prefix, chunk, dev) for l in range(L)]
+        ws, out = dw.prefill_buffers(chunk)
+        ws.view(torch.int32).fill_(-1)                       # garbage: the kernels never read unwritten bytes
+        i32 = lambda xs: torch.tensor(xs, dtype=torch.int32, device=dev)
+        sp, nn, to = i32([prefix]), i32([chunk]), i32([0])
+        qp, nq, qo = i32([prefix]), i32([chunk]), i32([0])
+
+    def step(timed=None):
+        for l in range(L):
+            kvq.kv_quant_append(dw.g, l, dw.cache.pool, dw.cache.ring, dw.page_table, sp, nn, to, chunk, ks[l], vs[l],
+                                dw.cache.status, stream.cuda_stream)
+            if timed is not None:
+                timed[l][0].record(stream)
+            kvq.paged_prefill_attn(dw.g, l, dw.cache.pool, dw.cache.ring, 0, dw.page_table, qp, nq, qo, chunk,
+                                   dw.seq_len, dw.max_seq_len, qs[l], dw.sm_scale, ws, out, dw.cache.status,
+                                   stream.cuda_stream)
+            if timed is not None:
+                timed[l][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+    stream.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    call_ms = []
+    steps = max(2, args.prefill_steps)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            step(ev)
+            stream.synchronize()
+            call_ms += [x.elapsed_time(y) for x, y in ev]
+        e1.record(stream)
+    stream.synchronize()
+    assert dw.cache.read_status() == 0, "device status flagged during prefill"
+    step_ms = e0.elapsed_time(e1) / steps
+    ms = statistics.median(call_ms)
+    flops = prefill_flops(prefix, chunk, wl.num_q_heads)
+    peak = 1925.0
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        pass
+    tflops = flops / (ms / 1000.0) / 1e12
+    return {"workload": f"prefill_27b: {chunk}-token chunk over a {prefix}-token 2-bit prefix, {L} layers, 24 q heads",
+            "ms_per_layer_attention": ms, "ms_per_step": step_ms, "flop_per_layer": flops, "tflops": tflops,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_source": "measured bf16 dense (fp16 MMA runs at the same rate)"},
+            "workspace": "filled with 0xFF before the timed steps, never zeroed"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--seed", type=int, default=0)
@@ -357,6 +440,9 @@ def main():
     ap.add_argument("--lanes", type=int, default=WORKLOAD["lanes"])
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-prefix", type=int, default=65536)
+    ap.add_argument("--prefill-steps", type=int, default=3)
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -33,17 +33,14 @@
 
 namespace kvq {
 
-constexpr int DEC_WARPS = 4;
 #ifndef KVQ_DEC_CTAS_PER_SM
 #define KVQ_DEC_CTAS_PER_SM 2
 #endif
-#ifndef KVQ_DEC_STAGES
-#define KVQ_DEC_STAGES 2
+#ifndef KVQ_DEC_PAIRS
+#define KVQ_DEC_PAIRS 4
 #endif
+constexpr int DEC_PAIRS = KVQ_DEC_PAIRS;               // warp pairs per CTA
 constexpr int DEC_CTAS_PER_SM = KVQ_DEC_CTAS_PER_SM;  // resident CTAs per SM the grid is sized for
-constexpr int DEC_STAGES = KVQ_DEC_STAGES;            // pages in flight per warp
-constexpr int STAGE_BYTES = 2 * HQ2B_BLOCK;  // K block + V block of one page, one layer/head
-constexpr int V_OFF = HQ2B_BLOCK;
 constexpr int MIN_PAGES_PER_WARP = 2;
 constexpr int DEC_MAX_SLOTS = 96;            // partial records per (lane, query head), at most
 constexpr int SPIN_LIMIT = 1 << 16;          // bounded mbarrier waits (x ~1 us hint)
@@ -92,29 +89,31 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
-// A-operand pairs straight from a code word.  x << 2 brings codes 0..3 of the low byte of each
-// 16-bit half to mantissa bits 2-3, 4-5, 6-7, 8-9; x >> 6 does the same for the high byte.
-// OR-ing in the exponent of 256, 64, 16 or 4 makes each half read exactly M + c; one HFMA2
-// (on the FMA pipe) then yields 2c - 3 (keys) or c (values) exactly.
-__device__ __forceinline__ uint32_t code_raw(uint32_t x, int pos) {
-  const uint32_t mask = pos == 0 ? 0x000C000Cu : pos == 1 ? 0x00300030u : pos == 2 ? 0x00C000C0u : 0x03000300u;
-  const uint32_t magic = pos == 0 ? 0x5C005C00u : pos == 1 ? 0x54005400u : pos == 2 ? 0x4C004C00u : 0x44004400u;
+// A-operand pairs straight from a code word.  A 16-bit half holding code byte(s) with the code
+// of position i at bits 2k + 2i, 2k + 2i + 1 reads as the fp16 number M + c once every other bit
+// is masked off and the exponent of M = 2^(10 - 2k - 2i) is OR-ed in (one LOP3); M + c is exact.
+//   keys:   k = 1 (the word shifted left by 2, or right by 6 for its high byte): M = 256, 64, 16, 4;
+//           the MMA takes M + c as is and a per-page correction removes the M + 1.5 part.
+//   values: k = 0 (the word as is, or shifted right by 8): M = 1024, 256, 64, 16; one HSUB2
+//           (FMA pipe) turns M + c into c exactly.
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask, uint32_t magic) {
   return (x & mask) | magic;
 }
-__device__ __forceinline__ uint32_t h2fma(uint32_t a, uint32_t b, uint32_t c) {
-  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b), *reinterpret_cast<__half2*>(&c));
+__device__ __forceinline__ uint32_t h2sub(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
   return *reinterpret_cast<uint32_t*>(&r);
 }
-// key code as 2c - 3: (M + c) * 2 - (2M + 3)
-__device__ __forceinline__ uint32_t code_k(uint32_t x, int pos) {
-  const uint32_t neg = pos == 0 ? 0xE006E006u : pos == 1 ? 0xD818D818u : pos == 2 ? 0xD060D060u : 0xC980C980u;
-  return h2fma(code_raw(x, pos), 0x40004000u, neg);
-}
-// value code as c: (M + c) * 1 - M
-__device__ __forceinline__ uint32_t code_v(uint32_t x, int pos) {
-  const uint32_t neg = pos == 0 ? 0xDC00DC00u : pos == 1 ? 0xD400D400u : pos == 2 ? 0xCC00CC00u : 0xC400C400u;
-  return h2fma(code_raw(x, pos), 0x3C003C00u, neg);
-}
+constexpr uint32_t KMASK0 = 0x000C000Cu;   // key code position i: KMASK0 << 2i after the shift
+constexpr uint32_t VMASK0 = 0x00030003u;   // value code position i: VMASK0 << 2i
+// fp16x2 bit patterns: M + 0 for keys (256, 64, 16, 4) and values (1024, 256, 64, 16), and the
+// key correction M + 1.5 (257.5, 65.5, 17.5, 5.5), all exact in fp16
+__constant__ uint32_t c_kmag[4] = {0x5C005C00u, 0x54005400u, 0x4C004C00u, 0x44004400u};
+__constant__ uint32_t c_kcor[4] = {0x5C065C06u, 0x54185418u, 0x4C604C60u, 0x45804580u};
+__constant__ uint32_t c_vmag[4] = {0x64006400u, 0x5C005C00u, 0x54005400u, 0x4C004C00u};
+
+// lazy rescale: the running max of a head moves only when a page max exceeds it by more than
+// RESCALE_LOG2 (log2 domain), so P <= 2^0.5 and P * s_v stays below 65,504 for any finite V
+constexpr float RESCALE_LOG2 = 0.5f;
 
 // 2^x for the softmax (x <= 0 or -inf); one MUFU.EX2, relative error ~2^-22
 __device__ __forceinline__ float ex2(float x) {
@@ -171,16 +170,56 @@ __device__ __forceinline__ void cursor_next(Cursor& cu, const int* pre, int H) {
   } while (cu.n == 0);
 }
 
-template <int STAGES>
-__global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_main(AttnArgs a) {
+// Exchange slot written by the Q.K warp and read by the P.V warp of a pair, one page each:
+// per thread P[4 m-tiles][4] (fp32, C-fragment layout of S^T), then (alpha0, alpha1, m0, m1).
+// Stored as [5 float4][32 lanes] so both sides access it without bank conflicts.
+constexpr int X_F4 = 5;
+constexpr int X_BYTES = X_F4 * 32 * 16;
+constexpr int QS_BYTES = 8 * 32 * 16;   // the Q.K warp's query pairs: [8 uint4][32 lanes]
+constexpr int PAIR_BYTES = 4 * HQ2B_BLOCK + 2 * X_BYTES + QS_BYTES;  // K ring 2, V ring 2, exchange 2, q
+enum { PB_KFULL = 0, PB_VFULL = 2, PB_XFULL = 4, PB_XEMPTY = 6, PB_COUNT = 8 };
+
+__device__ __forceinline__ void locate(int u0, const int* pre, int lanes, int H, Cursor& cu) {
+  int lo = 0, hi = lanes;  // invariant: H*pre[lo] <= u0 < H*pre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (H * pre[mid] <= u0) lo = mid;
+    else hi = mid;
+  }
+  cu.b = lo;
+  cu.n = pre[lo + 1] - pre[lo];
+  const int off = u0 - H * pre[lo];
+  cu.h = off / cu.n;
+  cu.p = off - cu.h * cu.n;
+}
+
+__device__ __forceinline__ bool page_phys(const CacheView& c, const Cursor& cu, int32_t& phys) {
+  phys = c.page_table[(int64_t)cu.b * c.max_pages + cu.p];
+  return phys >= 0 && phys < c.pool_pages;
+}
+
+// Warp pairs: warp w < DEC_PAIRS runs Q.K^T + softmax of a page, warp w + DEC_PAIRS runs its
+// P.V one page behind; both walk the same range of pages.  Each warp streams its own half of
+// every page (K block / V block, 4,608 B each) through a 2-slot TMA ring.
+__global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_main(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, cq = lane & 3;
-  uint8_t* ring_smem = smem + warp * STAGES * STAGE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DEC_WARPS * STAGES * STAGE_BYTES) + warp * STAGES;
-  int* pre = reinterpret_cast<int*>(smem + DEC_WARPS * STAGES * STAGE_BYTES + DEC_WARPS * STAGES * 8);
+  const int pair = warp % DEC_PAIRS;
+  const bool is_qk = warp < DEC_PAIRS;
+  uint8_t* pbase = smem + pair * PAIR_BYTES;
+  uint8_t* kring = pbase;                            // 2 x K block
+  uint8_t* vring = pbase + 2 * HQ2B_BLOCK;           // 2 x V block
+  float4* xring = reinterpret_cast<float4*>(pbase + 4 * HQ2B_BLOCK);
+  uint4* qsm = reinterpret_cast<uint4*>(pbase + 4 * HQ2B_BLOCK + 2 * X_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DEC_PAIRS * PAIR_BYTES) + pair * PB_COUNT;
+  int* pre = reinterpret_cast<int*>(smem + DEC_PAIRS * PAIR_BYTES + DEC_PAIRS * PB_COUNT * 8);
+  auto BAR = [&](int i) { return smem_u32(&bars[i]); };
+  // the combine kernel may be scheduled now: it does its own tail work first and waits for
+  // this grid's completion before it reads any partial
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
   // exclusive prefix of main pages over lanes
   if (warp == 0) {
@@ -201,194 +240,164 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
     }
     if (lane == 0) pre[0] = 0;
   }
-  if (lane == 0) {
-    for (int s = 0; s < STAGES; s++) mbar_init(smem_u32(&bars[s]), 1);
+  if (lane == 0 && is_qk) {
+    for (int i = 0; i < 2; i++) {
+      mbar_init(BAR(PB_KFULL + i), 1);
+      mbar_init(BAR(PB_VFULL + i), 1);
+      mbar_init(BAR(PB_XFULL + i), 1);
+      mbar_init(BAR(PB_XEMPTY + i), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
-
   const int units = H * pre[a.lanes];
   const int Wp = units_per_warp(units, a.grid_warps, a.min_wp);
-  const int gw = blockIdx.x * DEC_WARPS + warp;
-  const int u0 = gw * Wp;
+  const int gp = blockIdx.x * DEC_PAIRS + pair;
+  const int u0 = gp * Wp;
   const int u1 = min(u0 + Wp, units);
   if (u0 >= u1) return;
+  const int n_units = u1 - u0;
 
-  // locate u0: lane b with H*pre[b] <= u0 < H*pre[b+1]
   Cursor cu;
-  {
-    int lo = 0, hi = a.lanes;  // invariant: H*pre[lo] <= u0 < H*pre[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (H * pre[mid] <= u0) lo = mid;
-      else hi = mid;
-    }
-    cu.b = lo;
-    cu.n = pre[lo + 1] - pre[lo];
-    const int off = u0 - H * pre[lo];
-    cu.h = off / cu.n;
-    cu.p = off - cu.h * cu.n;
-  }
-  Cursor pc = cu;  // producer cursor, runs STAGES pages ahead
-  const int64_t pool_pages = c.pool_pages;
-  uint32_t valid = 0, phase = 0;
-  int produced = u0;
-
-  auto produce = [&](int slot) {
-    const int32_t phys = c.page_table[(int64_t)pc.b * c.max_pages + pc.p];
-    const bool ok = phys >= 0 && phys < pool_pages;
+  locate(u0, pre, a.lanes, H, cu);
+  // producer cursor (this warp's own ring), two pages ahead at most
+  Cursor pc = cu;
+  int produced = 0;
+  uint32_t valid = 0;
+  uint8_t* ring = is_qk ? kring : vring;
+  const int kv = is_qk ? 0 : 1;
+  const int full_bar = is_qk ? PB_KFULL : PB_VFULL;
+  auto produce = [&]() {
+    const int slot = produced & 1;
+    int32_t phys;
+    const bool ok = page_phys(c, pc, phys);
     if (ok) {
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, pc.h, 0);
-        tma_page(smem_u32(ring_smem + slot * STAGE_BYTES), src, STAGE_BYTES, smem_u32(&bars[slot]));
+        const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, pc.h, kv);
+        tma_page(smem_u32(ring + slot * HQ2B_BLOCK), src, HQ2B_BLOCK, BAR(full_bar + slot));
       }
       valid |= 1u << slot;
     } else {
       valid &= ~(1u << slot);
-      if (lane == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
+      if (lane == 0 && is_qk) flag(c.status, KVQ_STATUS_PAGE_OOB);
     }
-    ++produced;
-    if (produced < u1) cursor_next(pc, pre, H);
+    if (++produced < n_units) cursor_next(pc, pre, H);
   };
-#pragma unroll
-  for (int s = 0; s < STAGES; s++)
-    if (u0 + s < u1) produce(s);
+  produce();
+  if (n_units > 1) produce();
 
-  // per-thread state: heads e0 = 2*cq, e1 = 2*cq + 1 of the group
-  float O[16][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, Z00 = 0.f, Z01 = 0.f, Z10 = 0.f, Z11 = 0.f;
-  uint32_t qh[16][2];
-  const float sl2 = a.scale_log2;
-
-  auto reset = [&]() {
-#pragma unroll
-    for (int i = 0; i < 16; i++)
-#pragma unroll
-      for (int e = 0; e < 4; e++) O[i][e] = 0.f;
-    m0 = m1 = -INFINITY;
-    l0 = l1 = Z00 = Z01 = Z10 = Z11 = 0.f;
-  };
-  // q of head r of the group, dims 64cq .. 64cq+63, as fp16 pairs in the contraction order
-  auto load_q = [&](int b, int h) {
-    uint32_t w[32];
-    if (r < G) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + r) * D + 64 * cq);
-#pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const uint4 v = src[i];
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; i++) w[i] = 0u;
-    }
-    auto qf = [&](int e) { return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]); };
-#pragma unroll
-    for (int j = 0; j < 4; j++)
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const int d0 = 16 * j + i;
-        qh[4 * j + i][0] = pack_h2(qf(d0), qf(d0 + 8));
-        qh[4 * j + i][1] = pack_h2(qf(d0 + 4), qf(d0 + 12));
-      }
-  };
-  auto flush = [&](int b, int h) {
-    // complete the per-thread partial sums over the 8 row groups
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, o);
-      l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
-      Z00 += __shfl_xor_sync(0xFFFFFFFFu, Z00, o);
-      Z01 += __shfl_xor_sync(0xFFFFFFFFu, Z01, o);
-      Z10 += __shfl_xor_sync(0xFFFFFFFFu, Z10, o);
-      Z11 += __shfl_xor_sync(0xFFFFFFFFu, Z11, o);
-    }
-    const int segstart = H * pre[b] + h * (pre[b + 1] - pre[b]);
-    const int k = gw - segstart / Wp;
-#pragma unroll
-    for (int e = 0; e < 2; e++) {
-      const int head = 2 * cq + e;
-      if (head < G) {
-        const int64_t pidx = ((int64_t)b * Hq + h * G + head) * a.max_splits + k;
-        float* dst = a.ws_o + pidx * D;
-#pragma unroll
-        for (int hf = 0; hf < 2; hf++) {
-          const float z = hf == 0 ? (e == 0 ? Z00 : Z01) : (e == 0 ? Z10 : Z11);
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 8; i++) {
-            v[i] = O[8 * hf + i][e] + z;
-            v[8 + i] = O[8 * hf + i][2 + e] + z;
-          }
-          float4* d4 = reinterpret_cast<float4*>(dst + 128 * hf + 16 * r);
-#pragma unroll
-          for (int i = 0; i < 4; i++) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-        }
-        if (r == 0)
-          reinterpret_cast<float2*>(a.ws_ml)[pidx] = e == 0 ? make_float2(m0, l0) : make_float2(m1, l1);
-      }
-    }
-  };
-
-  reset();
-  load_q(cu.b, cu.h);
   bool timed_out = false;
-  for (int u = u0; u < u1; u++) {
-    const int slot = (u - u0) % STAGES;
-    if (valid & (1u << slot)) {
-      // every lane waits; the warp gives up together if any lane ran out of tries
-      const bool ok = mbar_wait(smem_u32(&bars[slot]), (phase >> slot) & 1u);
-      if (!__all_sync(0xFFFFFFFFu, ok)) {
-        timed_out = true;
-        break;
+  if (is_qk) {
+    // =========================================================== Q.K^T + softmax warp
+    float m0 = -INFINITY, m1 = -INFINITY;
+    const float sl2 = a.scale_log2;
+    uint32_t kmag[4], kcor[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      kmag[i] = c_kmag[i];
+      kcor[i] = c_kcor[i];
+    }
+    // q of head r of the group, dims 64cq .. 64cq+63, as the fp16 B-fragment pairs of k-steps
+    // 4jw + i: (d, d+8) and (d+4, d+12) with d = 16jw + i; kept in shared memory, one uint4 =
+    // the 4 k-steps' first pairs or second pairs of one jw
+    auto load_q = [&](int b, int h) {
+      uint32_t w[32];
+      if (r < G) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + r) * D + 64 * cq);
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+          const uint4 v = src[i];
+          w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) w[i] = 0u;
       }
-      phase ^= 1u << slot;
-      const uint8_t* st = ring_smem + slot * STAGE_BYTES;
-
-      // ---- S^T for the four 16-token m-tiles.  k-step ks = 4j + i of thread column cq covers
-      // dims 64cq + 16j + {i, i+8} (A regs 0/1: codes of bytes 0/2 of word j) and
-      // {i+4, i+12} (A regs 2/3: bytes 1/3); q~ = q (.) s_page is formed per word j from the
-      // natural-order scale pairs.
+      auto qf = [&](int e) { return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]); };
+#pragma unroll
+      for (int jw = 0; jw < 4; jw++) {
+        uint32_t p0[4], p1[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const int d0 = 16 * jw + i;
+          p0[i] = pack_h2(qf(d0), qf(d0 + 8));
+          p1[i] = pack_h2(qf(d0 + 4), qf(d0 + 12));
+        }
+        qsm[(2 * jw) * 32 + lane] = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+        qsm[(2 * jw + 1) * 32 + lane] = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+      }
+      __syncwarp();
+    };
+    load_q(cu.b, cu.h);
+    for (int j = 0; j < n_units; j++) {
+      const int slot = j & 1;
+      const uint32_t par = (j >> 1) & 1;
       float S[4][4];
 #pragma unroll
       for (int mt = 0; mt < 4; mt++)
 #pragma unroll
-        for (int e = 0; e < 4; e++) S[mt][e] = 0.f;
-      const uint8_t* krow_a = st + perm_row(r) * HQ2B_ROW + 16 * cq;
-      const uint8_t* krow_b = st + (8 + perm_row(r)) * HQ2B_ROW + 16 * cq;
-      const uint8_t* kscale = st + HQ2B_META_OFF + 128 * cq;
+        for (int e = 0; e < 4; e++) S[mt][e] = -INFINITY;
+      if (valid & (1u << slot)) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_KFULL + slot), par))) { timed_out = true; break; }
+        const uint8_t* st = kring + slot * HQ2B_BLOCK;
+        float Cc[4] = {0.f, 0.f, 0.f, 0.f};   // sum over dims of q~ (M + 1.5): the same for every key
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        const uint4 s_lo = *reinterpret_cast<const uint4*>(kscale + 32 * j);       // dims 16j .. 16j+7
-        const uint4 s_hi = *reinterpret_cast<const uint4*>(kscale + 32 * j + 16);  // dims 16j+8 .. 16j+15
-        const uint32_t slo[4] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w};
-        const uint32_t shi[4] = {s_hi.x, s_hi.y, s_hi.z, s_hi.w};
-        uint32_t bq[4][2];
+        for (int mt = 0; mt < 4; mt++)
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-          bq[i][0] = h2mul(qh[4 * j + i][0], __byte_perm(slo[i >> 1], shi[i >> 1], sel));
-          bq[i][1] = h2mul(qh[4 * j + i][1], __byte_perm(slo[2 + (i >> 1)], shi[2 + (i >> 1)], sel));
+          for (int e = 0; e < 4; e++) S[mt][e] = 0.f;
+        // k-step ks = 4j + i of thread column cq covers dims 64cq + 16j + {i, i+8} (A regs 0/1:
+        // codes of bytes 0/2 of word j) and {i+4, i+12} (A regs 2/3: bytes 1/3)
+        const uint8_t* krow_a = st + perm_row(r) * HQ2B_ROW + 16 * cq;
+        const uint8_t* krow_b = st + (8 + perm_row(r)) * HQ2B_ROW + 16 * cq;
+        const uint8_t* kscale = st + HQ2B_META_OFF + 128 * cq;
+#pragma unroll
+        for (int jw = 0; jw < 4; jw++) {
+          const uint4 s_lo = *reinterpret_cast<const uint4*>(kscale + 32 * jw);
+          const uint4 s_hi = *reinterpret_cast<const uint4*>(kscale + 32 * jw + 16);
+          const uint32_t slo[4] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w};
+          const uint32_t shi[4] = {s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+          const uint4 qa = qsm[(2 * jw) * 32 + lane], qb = qsm[(2 * jw + 1) * 32 + lane];
+          const uint32_t q0[4] = {qa.x, qa.y, qa.z, qa.w}, q1[4] = {qb.x, qb.y, qb.z, qb.w};
+          uint32_t bq[4][2];
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+            bq[i][0] = h2mul(q0[i], __byte_perm(slo[i >> 1], shi[i >> 1], sel));
+            bq[i][1] = h2mul(q1[i], __byte_perm(slo[2 + (i >> 1)], shi[2 + (i >> 1)], sel));
+            mma16816(Cc, kcor[i], kcor[i], kcor[i], kcor[i], bq[i][0], bq[i][1]);
+          }
+#pragma unroll
+          for (int mt = 0; mt < 4; mt++) {
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(krow_a + 16 * mt * HQ2B_ROW + 4 * jw);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(krow_b + 16 * mt * HQ2B_ROW + 4 * jw);
+            const uint32_t la = wa << 2, ra = wa >> 6, lb = wb << 2, rb = wb >> 6;
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+              const uint32_t mk = KMASK0 << (2 * i);
+              mma16816(S[mt], lop_and_or(la, mk, kmag[i]), lop_and_or(lb, mk, kmag[i]), lop_and_or(ra, mk, kmag[i]),
+                       lop_and_or(rb, mk, kmag[i]), bq[i][0], bq[i][1]);
+            }
+          }
         }
+        // q~ . k^ = 2 (sum q~ (M + c) - sum q~ (M + 1.5)), then the softmax scale (log2 domain)
+        const float k2 = 2.f * sl2;
+        const float cn0 = -Cc[0] * k2, cn1 = -Cc[1] * k2;
 #pragma unroll
         for (int mt = 0; mt < 4; mt++) {
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(krow_a + 16 * mt * HQ2B_ROW + 4 * j);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(krow_b + 16 * mt * HQ2B_ROW + 4 * j);
-          const uint32_t la = wa << 2, ra = wa >> 6, lb = wb << 2, rb = wb >> 6;
-#pragma unroll
-          for (int i = 0; i < 4; i++)
-            mma16816(S[mt], code_k(la, i), code_k(lb, i), code_k(ra, i), code_k(rb, i), bq[i][0], bq[i][1]);
+          S[mt][0] = fmaf(S[mt][0], k2, cn0);
+          S[mt][1] = fmaf(S[mt][1], k2, cn1);
+          S[mt][2] = fmaf(S[mt][2], k2, cn0);
+          S[mt][3] = fmaf(S[mt][3], k2, cn1);
         }
       }
-      // ---- online softmax (log2 domain)
+      __syncwarp();
+      // the K slot is free: refill it two pages ahead
+      if (produced < n_units) produce();
+      // ---- online softmax (log2 domain): page max per head, P relative to the running max
       float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
       for (int mt = 0; mt < 4; mt++) {
-        S[mt][0] *= sl2;
-        S[mt][1] *= sl2;
-        S[mt][2] *= sl2;
-        S[mt][3] *= sl2;
         mx0 = fmaxf(mx0, fmaxf(S[mt][0], S[mt][2]));
         mx1 = fmaxf(mx1, fmaxf(S[mt][1], S[mt][3]));
       }
@@ -397,22 +406,61 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
       }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < 4; mt++) {
-        S[mt][0] = ex2(S[mt][0] - mn0);
-        S[mt][1] = ex2(S[mt][1] - mn1);
-        S[mt][2] = ex2(S[mt][2] - mn0);
-        S[mt][3] = ex2(S[mt][3] - mn1);
-        ps0 += S[mt][0] + S[mt][2];
-        ps1 += S[mt][1] + S[mt][3];
+      // lazy rescale: move a head's max only when the page max passes it by RESCALE_LOG2
+      float al0 = 1.f, al1 = 1.f;
+      if (mx0 > m0 + RESCALE_LOG2) {
+        if (m0 != -INFINITY) al0 = ex2(m0 - mx0);
+        m0 = mx0;
       }
-      l0 = fmaf(l0, al0, ps0);
-      l1 = fmaf(l1, al1, ps1);
+      if (mx1 > m1 + RESCALE_LOG2) {
+        if (m1 != -INFINITY) al1 = ex2(m1 - mx1);
+        m1 = mx1;
+      }
+      const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
+      float4 px[4];
+#pragma unroll
+      for (int mt = 0; mt < 4; mt++)
+        px[mt] = make_float4(ex2(S[mt][0] - mu0), ex2(S[mt][1] - mu1), ex2(S[mt][2] - mu0), ex2(S[mt][3] - mu1));
+      // ---- hand P, alpha and m to the P.V warp
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_XEMPTY + slot), par ^ 1u))) { timed_out = true; break; }
+      float4* xs = xring + slot * (X_F4 * 32);
+#pragma unroll
+      for (int mt = 0; mt < 4; mt++) xs[mt * 32 + lane] = px[mt];
+      xs[4 * 32 + lane] = make_float4(al0, al1, m0, m1);
+      __syncwarp();
+      if (lane == 0) asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(BAR(PB_XFULL + slot)) : "memory");
+      // next (lane, head) segment: fresh max, new query
+      if (j + 1 < n_units) {
+        if (cu.p + 1 == cu.n) {
+          cursor_next(cu, pre, H);
+          m0 = m1 = -INFINITY;
+          load_q(cu.b, cu.h);
+        } else {
+          cursor_next(cu, pre, H);
+        }
+      }
+    }
+  } else {
+    // =========================================================== P.V warp
+    float O[16][4];
+    float l0 = 0.f, l1 = 0.f, Z00 = 0.f, Z01 = 0.f, Z10 = 0.f, Z11 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; i++)
+#pragma unroll
+      for (int e = 0; e < 4; e++) O[i][e] = 0.f;
+    const int t0 = perm_row(2 * cq), t1 = perm_row(2 * cq + 1);
+    uint32_t vmag[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) vmag[i] = c_vmag[i];
+    for (int j = 0; j < n_units; j++) {
+      const int slot = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_XFULL + slot), par))) { timed_out = true; break; }
+      // P of the page is read per m-tile below; the slot is released after the page
+      const float4* xs = xring + slot * (X_F4 * 32);
+      const float4 am = xs[4 * 32 + lane];
+      const float al0 = am.x, al1 = am.y;
+      l0 *= al0; l1 *= al1;
       Z00 *= al0; Z10 *= al0; Z01 *= al1; Z11 *= al1;
       if (__any_sync(0xFFFFFFFFu, al0 != 1.0f || al1 != 1.0f)) {
 #pragma unroll
@@ -420,98 +468,146 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, DEC_CTAS_PER_SM) decode_hq2b_m
           O[i][0] *= al0; O[i][1] *= al1; O[i][2] *= al0; O[i][3] *= al1;
         }
       }
-      // ---- P (.) s_v per half, sum(P z), and the B fragments of P.V
-      uint32_t Bv[2][4][2];
+      if (valid & (1u << slot)) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_VFULL + slot), par))) { timed_out = true; break; }
+        const uint8_t* st = vring + slot * HQ2B_BLOCK;
+        // per m-tile: P (.) s_v per half (fp16), sum(P z), sum(P), the B fragments, then
+        // O^T += V^ . P'^T with a fp16 pair holding one dim of two tokens as the exact code c
 #pragma unroll
-      for (int mt = 0; mt < 4; mt++) {
+        for (int mt = 0; mt < 4; mt++) {
+          const float4 pxm = xs[mt * 32 + lane];
+          const float pv[4] = {pxm.x, pxm.y, pxm.z, pxm.w};
+          uint32_t Bv[2][2];
 #pragma unroll
-        for (int rr = 0; rr < 2; rr++) {
-          const int tok = 16 * mt + 8 * rr + perm_row(r);
-          const uint2 mw = *reinterpret_cast<const uint2*>(st + V_OFF + HQ2B_META_OFF + tok * 8);
-          const float s0 = half_bits_to_float((uint16_t)(mw.x & 0xFFFFu));
-          const float z0 = half_bits_to_float((uint16_t)(mw.x >> 16));
-          const float s1 = half_bits_to_float((uint16_t)(mw.y & 0xFFFFu));
-          const float z1 = half_bits_to_float((uint16_t)(mw.y >> 16));
-          const float pa = S[mt][2 * rr], pb = S[mt][2 * rr + 1];
-          Z00 = fmaf(pa, z0, Z00);
-          Z01 = fmaf(pb, z0, Z01);
-          Z10 = fmaf(pa, z1, Z10);
-          Z11 = fmaf(pb, z1, Z11);
-          Bv[0][mt][rr] = movmatrix_t(pack_h2(pa * s0, pb * s0));
-          Bv[1][mt][rr] = movmatrix_t(pack_h2(pa * s1, pb * s1));
-        }
-      }
-      // ---- O^T += V^ . P'^T: a fp16 pair holds one dim of two tokens (bytes permuted so each
-      // half of a word is one token) as the exact code c
-      const int t0 = perm_row(2 * cq), t1 = perm_row(2 * cq + 1);
-#pragma unroll
-      for (int mt = 0; mt < 4; mt++) {
-#pragma unroll
-        for (int hf = 0; hf < 2; hf++) {
-          const uint8_t* vb = st + V_OFF + 32 * hf + 4 * r;
-          const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + t0) * HQ2B_ROW);
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + t1) * HQ2B_ROW);
-          const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t0) * HQ2B_ROW);
-          const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t1) * HQ2B_ROW);
-          // [tok_a byte k, tok_a byte k+1, tok_b byte k, tok_b byte k+1], k = 0 (dims 16r..16r+7) or 2 (+8)
-          const uint32_t x[4] = {__byte_perm(w0, w1, 0x5410u), __byte_perm(w0, w1, 0x7632u),
-                                 __byte_perm(w2, w3, 0x5410u), __byte_perm(w2, w3, 0x7632u)};
-          uint32_t lo[4], hi[4];
-#pragma unroll
-          for (int k = 0; k < 4; k++) {
-            lo[k] = x[k] << 2;  // codes of the first byte of each half
-            hi[k] = x[k] >> 6;  // codes of the second byte
+          for (int rr = 0; rr < 2; rr++) {
+            const int tok = 16 * mt + 8 * rr + perm_row(r);
+            const uint2 mw = *reinterpret_cast<const uint2*>(st + HQ2B_META_OFF + tok * 8);
+            const float z0 = half_bits_to_float((uint16_t)(mw.x >> 16));
+            const float z1 = half_bits_to_float((uint16_t)(mw.y >> 16));
+            const float pa = pv[2 * rr], pb = pv[2 * rr + 1];
+            l0 += pa;
+            l1 += pb;
+            Z00 = fmaf(pa, z0, Z00);
+            Z01 = fmaf(pb, z0, Z01);
+            Z10 = fmaf(pa, z1, Z10);
+            Z11 = fmaf(pb, z1, Z11);
+            const __half2 p2 = __floats2half2_rn(pa, pb);
+            const __half2 s0 = __low2half2(*reinterpret_cast<const __half2*>(&mw.x));
+            const __half2 s1 = __low2half2(*reinterpret_cast<const __half2*>(&mw.y));
+            const __half2 b0 = __hmul2(p2, s0), b1 = __hmul2(p2, s1);
+            Bv[0][rr] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&b0));
+            Bv[1][rr] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&b1));
           }
 #pragma unroll
-          for (int i8 = 0; i8 < 8; i8++) {
-            const int pos = i8 & 3;
-            const uint32_t* src = i8 < 4 ? lo : hi;
-            mma16816(O[8 * hf + i8], code_v(src[0], pos), code_v(src[1], pos), code_v(src[2], pos),
-                     code_v(src[3], pos), Bv[hf][mt][0], Bv[hf][mt][1]);
+          for (int hf = 0; hf < 2; hf++) {
+            const uint8_t* vb = st + 32 * hf + 4 * r;
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + t0) * HQ2B_ROW);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + t1) * HQ2B_ROW);
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t0) * HQ2B_ROW);
+            const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t1) * HQ2B_ROW);
+            const uint32_t x[4] = {__byte_perm(w0, w1, 0x5410u), __byte_perm(w0, w1, 0x7632u),
+                                   __byte_perm(w2, w3, 0x5410u), __byte_perm(w2, w3, 0x7632u)};
+            uint32_t hi[4];
+#pragma unroll
+            for (int k = 0; k < 4; k++) hi[k] = x[k] >> 8;
+#pragma unroll
+            for (int i8 = 0; i8 < 8; i8++) {
+              const int pos = i8 & 3;
+              const uint32_t* src = i8 < 4 ? x : hi;
+              const uint32_t mk = VMASK0 << (2 * pos);
+              mma16816(O[8 * hf + i8], h2sub(lop_and_or(src[0], mk, vmag[pos]), vmag[pos]),
+                       h2sub(lop_and_or(src[1], mk, vmag[pos]), vmag[pos]),
+                       h2sub(lop_and_or(src[2], mk, vmag[pos]), vmag[pos]),
+                       h2sub(lop_and_or(src[3], mk, vmag[pos]), vmag[pos]), Bv[hf][0], Bv[hf][1]);
+            }
           }
         }
       }
       __syncwarp();
-    }
-    // refill this slot with the page STAGES ahead
-    if (produced < u1) produce(slot);
-    // segment boundary: flush and start the next (lane, head)
-    const bool last = (u + 1 == u1);
-    if (last || cu.p + 1 == cu.n) {
-      flush(cu.b, cu.h);
-      if (!last) {
+      if (lane == 0) asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(BAR(PB_XEMPTY + slot)) : "memory");
+      if (produced < n_units) produce();
+      // segment end: write this pair's partial (m, l, O + z-term) and start afresh
+      const bool last = (j + 1 == n_units);
+      if (last || cu.p + 1 == cu.n) {
+        float ls0 = l0, ls1 = l1, z00 = Z00, z01 = Z01, z10 = Z10, z11 = Z11;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, o);
+          ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, o);
+          z00 += __shfl_xor_sync(0xFFFFFFFFu, z00, o);
+          z01 += __shfl_xor_sync(0xFFFFFFFFu, z01, o);
+          z10 += __shfl_xor_sync(0xFFFFFFFFu, z10, o);
+          z11 += __shfl_xor_sync(0xFFFFFFFFu, z11, o);
+        }
+        const int segstart = H * pre[cu.b] + cu.h * (pre[cu.b + 1] - pre[cu.b]);
+        const int k = gp - segstart / Wp;
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          const int head = 2 * cq + e;
+          if (head < G) {
+            const int64_t pidx = ((int64_t)cu.b * Hq + cu.h * G + head) * a.max_splits + k;
+            float* dst = a.ws_o + pidx * D;
+#pragma unroll
+            for (int hf = 0; hf < 2; hf++) {
+              const float z = hf == 0 ? (e == 0 ? z00 : z01) : (e == 0 ? z10 : z11);
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 8; i++) {
+                v[i] = O[8 * hf + i][e] + z;
+                v[8 + i] = O[8 * hf + i][2 + e] + z;
+              }
+              float4* d4 = reinterpret_cast<float4*>(dst + 128 * hf + 16 * r);
+#pragma unroll
+              for (int i = 0; i < 4; i++) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            }
+            if (r == 0)
+              reinterpret_cast<float2*>(a.ws_ml)[pidx] = e == 0 ? make_float2(am.z, ls0) : make_float2(am.w, ls1);
+          }
+        }
+        if (!last) {
+          cursor_next(cu, pre, H);
+#pragma unroll
+          for (int i = 0; i < 16; i++)
+#pragma unroll
+            for (int e = 0; e < 4; e++) O[i][e] = 0.f;
+          l0 = l1 = Z00 = Z01 = Z10 = Z11 = 0.f;
+        }
+      } else {
         cursor_next(cu, pre, H);
-        reset();
-        load_q(cu.b, cu.h);
       }
-    } else {
-      cursor_next(cu, pre, H);
     }
   }
-  if (timed_out) {
-    if (lane == 0) flag(c.status, KVQ_STATUS_TIMEOUT);
-    // let copies still in flight land before the CTA's shared memory is released
-    for (int s = 0; s < STAGES; s++)
-      if (valid & (1u << s)) mbar_wait(smem_u32(&bars[s]), (phase >> s) & 1u);
-  }
+  if (timed_out && lane == 0) flag(c.status, KVQ_STATUS_TIMEOUT);
+  // copies still in flight into this warp's ring must land before the CTA's smem is released
+  for (int q = max(0, produced - 2); q < produced; q++)
+    if (valid & (1u << (q & 1))) mbar_wait(BAR(full_bar + (q & 1)), (q >> 1) & 1u);
 }
 
 // ----------------------------------------------------------------------------- combine + tail
-// One CTA per (lane, query head): attends the exact tail [tail_start, len) on CUDA cores
-// (keys from the ring past exact_from, else from the page codes) and merges it with the
-// main-path partials of this (lane, head) in FP32.
+// One CTA per (lane, query head).  Part 1 attends the exact tail [tail_start, len) on CUDA
+// cores -- keys from the ring past exact_from, else from the closed page's codes; values from
+// the page codes -- and needs nothing from the main kernel, so it runs while the main grid
+// drains (programmatic dependent launch).  Part 2 waits for the main grid and merges its
+// partials of this (lane, head) with the tail in FP32.
+constexpr int TAIL_MAX = 2 * P;   // len - tail_start < 2 pages, since the window is at most a page
+
 __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
   const int b = blockIdx.x, j = blockIdx.y, h = j / G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ __align__(16) float s_p[TAIL_MAX];                // tail scores, then probabilities
+  __shared__ __align__(16) uint8_t s_vc[TAIL_MAX][HQ2B_ROW];  // tail V codes
+  __shared__ __align__(16) uint32_t s_vm[TAIL_MAX][2];        // tail V meta (s0 z0, s1 z1)
+  __shared__ __align__(16) float s_red[4][D];
+  __shared__ float s_w[DEC_MAX_SLOTS];
+  __shared__ float s_tail[2], s_fin[2];
+  __shared__ int32_t s_phys[2];
   __shared__ int s_sum[2][8];
-  __shared__ float wm[8], wl[8];
-  __shared__ __align__(16) float wacc[8][D];
 
   // main pages of lanes before b, and of all lanes
   int before = 0, total = 0;
-  for (int i = threadIdx.x; i < a.lanes; i += blockDim.x) {
+  for (int i = tid; i < a.lanes; i += blockDim.x) {
     const int n = main_pages(c, a.seq_len, i);
     total += n;
     if (i < b) before += n;
@@ -525,6 +621,24 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
     s_sum[0][warp] = before;
     s_sum[1][warp] = total;
   }
+  const int len = a.seq_len[b];
+  const bool bad = len < 0 || len > c.max_pages * P;
+  const int npg = bad ? 0 : main_pages(c, a.seq_len, b);
+  const int ef = bad ? 0 : exact_from(len, c.window);
+  const int tail_start = npg * P;
+  const int ntail = bad ? 0 : len - tail_start;
+  if (tid < 2) {
+    const int p = tail_start / P + tid;
+    int32_t phys = -1;
+    if (!bad && p * P < len) {
+      phys = c.page_table[(int64_t)b * c.max_pages + p];
+      if (phys < 0 || phys >= c.pool_pages) {
+        if (j % G == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
+        phys = -1;
+      }
+    }
+    s_phys[tid] = phys;
+  }
   __syncthreads();
   before = 0;
   total = 0;
@@ -533,17 +647,26 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
     before += s_sum[0][w];
     total += s_sum[1][w];
   }
-  float* out = a.out + ((int64_t)b * Hq + j) * D;
-  const int len = a.seq_len[b];
-  if (len < 0 || len > c.max_pages * P) {
-    out[threadIdx.x] = 0.f;
-    return;
-  }
-  const int npg = main_pages(c, a.seq_len, b);
-  const int ef = exact_from(len, c.window);
-  const int tail_start = npg * P;
 
-  // ---- tail on CUDA cores: warp w takes tokens tail_start + w, + 8, ...
+  // ---- part 1a: tail V rows to shared memory (64 B codes + 8 B meta each)
+  for (int i = tid; i < ntail * 4; i += blockDim.x) {
+    const int t = i >> 2, pos = tail_start + t;
+    const int32_t phys = s_phys[pos / P - tail_start / P];
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (phys >= 0) {
+      const uint8_t* vblk = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 1);
+      w = reinterpret_cast<const uint4*>(vblk + (pos % P) * HQ2B_ROW)[i & 3];
+      if ((i & 3) == 0) {
+        const uint2 m = *reinterpret_cast<const uint2*>(vblk + HQ2B_META_OFF + (pos % P) * 8);
+        s_vm[t][0] = m.x;
+        s_vm[t][1] = m.y;
+      }
+    } else if ((i & 3) == 0) {
+      s_vm[t][0] = s_vm[t][1] = 0u;
+    }
+    reinterpret_cast<uint4*>(s_vc[t])[i & 3] = w;
+  }
+  // ---- part 1b: tail scores; warp w takes keys w, w + 8, ..., four at a time, lanes over dims
   float q[8];
   {
     const uint4 w4 = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + j) * D)[lane];
@@ -554,97 +677,175 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
       q[2 * i + 1] = bf16_hi(u[i]) * a.scale_log2;
     }
   }
-  float m = -INFINITY, l = 0.f, acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; i++) acc[i] = 0.f;
-  bool oob = false;
-  for (int t = tail_start + warp; t < len; t += 8) {
-    const int32_t phys = c.page_table[(int64_t)b * c.max_pages + t / P];
-    if (phys < 0 || phys >= c.pool_pages) {
-      oob = true;
-      continue;
+  // K channel scales of the closed page the tail starts in (dims 8 lane .. 8 lane + 7)
+  float ks[8];
+  const uint8_t* kblk0 = nullptr;
+  {
+    uint4 sw = make_uint4(0u, 0u, 0u, 0u);
+    if (tail_start < ef && s_phys[0] >= 0) {
+      kblk0 = c.pool + (int64_t)s_phys[0] * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
+      sw = reinterpret_cast<const uint4*>(kblk0 + HQ2B_META_OFF)[lane];
     }
-    const uint8_t* page = c.pool + (int64_t)phys * c.page_bytes;
-    const uint8_t* kblk = page + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
-    const uint8_t* vblk = kblk + HQ2B_BLOCK;
-    const int slot = t % P;
-    float kx[8];
-    if (t >= ef) {
-      const uint4 w4 = reinterpret_cast<const uint4*>(c.ring + ring_row_offset(c, b, h, slot))[lane];
-      const uint32_t u[4] = {w4.x, w4.y, w4.z, w4.w};
+    const __half2* sc = reinterpret_cast<const __half2*>(&sw);
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        kx[2 * i] = bf16_lo(u[i]);
-        kx[2 * i + 1] = bf16_hi(u[i]);
-      }
-    } else {
-      const uint32_t codes = reinterpret_cast<const uint16_t*>(kblk + slot * HQ2B_ROW)[lane];
-      const uint4 sw = reinterpret_cast<const uint4*>(kblk + HQ2B_META_OFF)[lane];
-      const __half2* sc = reinterpret_cast<const __half2*>(&sw);
+    for (int i = 0; i < 4; i++) {
+      const float2 f = __half22float2(sc[i]);
+      ks[2 * i] = f.x;
+      ks[2 * i + 1] = f.y;
+    }
+  }
+  for (int t0 = warp; t0 < ntail; t0 += 32) {
+    float dot[4];
+    uint4 kw[4];
 #pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const float2 sp = __half22float2(sc[i]);
-        kx[2 * i] = sp.x * (float)(2 * (int)((codes >> (4 * i)) & 3) - 3);
-        kx[2 * i + 1] = sp.y * (float)(2 * (int)((codes >> (4 * i + 2)) & 3) - 3);
+    for (int u = 0; u < 4; u++) {             // loads of four keys in flight
+      const int t = t0 + 8 * u, pos = tail_start + t;
+      kw[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (t < ntail) {
+        if (pos >= ef)
+          kw[u] = reinterpret_cast<const uint4*>(c.ring + ring_row_offset(c, b, h, pos % P))[lane];
+        else if (kblk0)
+          kw[u].x = reinterpret_cast<const uint16_t*>(kblk0 + (pos % P) * HQ2B_ROW)[lane];
       }
     }
-    float dot = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; i++) dot = fmaf(q[i], kx[i], dot);
+    for (int u = 0; u < 4; u++) {
+      const int pos = tail_start + t0 + 8 * u;
+      float kx[8];
+      if (pos >= ef) {
+        const uint32_t w[4] = {kw[u].x, kw[u].y, kw[u].z, kw[u].w};
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) dot += __shfl_xor_sync(0xFFFFFFFFu, dot, o);
-    const uint32_t codes = reinterpret_cast<const uint16_t*>(vblk + slot * HQ2B_ROW)[lane];
-    const uint32_t meta = reinterpret_cast<const uint32_t*>(vblk + HQ2B_META_OFF + slot * 8)[lane >> 4];
-    const float sv = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
-    const float zv = half_bits_to_float((uint16_t)(meta >> 16));
-    const float mn = fmaxf(m, dot);
-    const float al = exp2f(m - mn), p = exp2f(dot - mn);
-    m = mn;
-    l = fmaf(l, al, p);
+        for (int i = 0; i < 4; i++) {
+          kx[2 * i] = bf16_lo(w[i]);
+          kx[2 * i + 1] = bf16_hi(w[i]);
+        }
+      } else {
 #pragma unroll
-    for (int i = 0; i < 8; i++) acc[i] = fmaf(acc[i], al, p * (zv + (float)((codes >> (2 * i)) & 3) * sv));
+        for (int i = 0; i < 8; i++) kx[i] = ks[i] * (float)(2 * (int)((kw[u].x >> (2 * i)) & 3u) - 3);
+      }
+      float d = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; i++) d = fmaf(q[i], kx[i], d);
+      dot[u] = d;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < 4; u++) dot[u] += __shfl_xor_sync(0xFFFFFFFFu, dot[u], o);
+    if (lane < 4 && t0 + 8 * lane < ntail) {
+      float v = dot[0];
+#pragma unroll
+      for (int u = 1; u < 4; u++) v = lane == u ? dot[u] : v;
+      s_p[t0 + 8 * lane] = v;
+    }
   }
-  if (oob && lane == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
-  if (lane == 0) {
-    wm[warp] = m;
-    wl[warp] = l;
-  }
-  reinterpret_cast<float4*>(&wacc[warp][8 * lane])[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-  reinterpret_cast<float4*>(&wacc[warp][8 * lane])[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   __syncthreads();
+  // ---- part 1c: tail softmax (log2 domain), warp 0
+  if (warp == 0) {
+    float x[TAIL_MAX / 32];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < TAIL_MAX / 32; i++) {
+      const int t = lane + 32 * i;
+      x[i] = t < ntail ? s_p[t] : -INFINITY;
+      m = fmaxf(m, x[i]);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float l = 0.f;
+#pragma unroll
+    for (int i = 0; i < TAIL_MAX / 32; i++) {
+      const float p = x[i] == -INFINITY ? 0.f : exp2f(x[i] - m);
+      s_p[lane + 32 * i] = p;
+      l += p;
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) l += __shfl_xor_sync(0xFFFFFFFFu, l, o);
+    if (lane == 0) {
+      s_tail[0] = m;
+      s_tail[1] = l;
+    }
+  }
+  __syncthreads();
+  // ---- part 1d: tail P.V, thread = dim
+  const int d = tid;
+  float acc = 0.f;
+  {
+    const int hf = d >> 7, shift = 2 * (d & 3), byte = d >> 2;
+#pragma unroll 8
+    for (int t = 0; t < ntail; t++) {
+      const uint32_t mw = s_vm[t][hf];
+      const float sv = half_bits_to_float((uint16_t)(mw & 0xFFFFu));
+      const float zv = half_bits_to_float((uint16_t)(mw >> 16));
+      acc = fmaf(s_p[t], fmaf((float)((s_vc[t][byte] >> shift) & 3u), sv, zv), acc);
+    }
+  }
 
-  // ---- merge: main partials of this (lane, head) + the 8 tail warps
-  const int d = threadIdx.x;
+  // ---- part 2: the main partials are complete once the main grid is
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   int nk = 0;
-  int64_t p0 = 0;
   if (npg > 0) {
     const int units = H * total;
     const int Wp = units_per_warp(units, a.grid_warps, a.min_wp);
     const int segstart = H * before + h * npg;
     nk = (segstart + npg - 1) / Wp - segstart / Wp + 1;
-    p0 = ((int64_t)b * Hq + j) * a.max_splits;
   }
-  const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + p0;
-  float M = -INFINITY;
-#pragma unroll 8
-  for (int k = 0; k < nk; k++) M = fmaxf(M, ml[k].x);
+  const int64_t pbase = ((int64_t)b * Hq + j) * a.max_splits;
+  if (warp == 0) {
+    const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + pbase;
+    float mk[DEC_MAX_SLOTS / 32], lk[DEC_MAX_SLOTS / 32];
+    float M = s_tail[0];
 #pragma unroll
-  for (int w = 0; w < 8; w++) M = fmaxf(M, wm[w]);
-  float num = 0.f, den = 0.f;
-#pragma unroll 8
-  for (int k = 0; k < nk; k++) {
-    const float2 e = ml[k];
-    const float w = e.x == -INFINITY ? 0.f : exp2f(e.x - M);
-    den = fmaf(e.y, w, den);
-    num = fmaf(a.ws_o[(p0 + k) * D + d], w, num);
-  }
+    for (int i = 0; i < DEC_MAX_SLOTS / 32; i++) {
+      const int k = lane + 32 * i;
+      mk[i] = -INFINITY;
+      lk[i] = 0.f;
+      if (k < nk) {
+        const float2 e = ml[k];
+        mk[i] = e.x;
+        lk[i] = e.y;
+      }
+      M = fmaxf(M, mk[i]);
+    }
 #pragma unroll
-  for (int w = 0; w < 8; w++) {
-    const float e = wm[w] == -INFINITY ? 0.f : exp2f(wm[w] - M);
-    den = fmaf(wl[w], e, den);
-    num = fmaf(wacc[w][d], e, num);
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    float den = 0.f;
+#pragma unroll
+    for (int i = 0; i < DEC_MAX_SLOTS / 32; i++) {
+      const int k = lane + 32 * i;
+      const float w = mk[i] == -INFINITY ? 0.f : exp2f(mk[i] - M);
+      if (k < nk) s_w[k] = w;
+      den = fmaf(lk[i], w, den);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xFFFFFFFFu, den, o);
+    if (lane == 0) {
+      const float wt = s_tail[0] == -INFINITY ? 0.f : exp2f(s_tail[0] - M);
+      s_fin[0] = wt;
+      s_fin[1] = fmaf(s_tail[1], wt, den);
+    }
   }
-  out[d] = den > 0.f ? num / den : 0.f;
+  __syncthreads();
+  // partial k goes to thread group k % 4; each thread sums 4 dims of its group's partials
+  {
+    const int dq = tid & 63, kg = tid >> 6;
+    const float4* part = reinterpret_cast<const float4*>(a.ws_o + pbase * D) + dq;
+    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int k = kg; k < nk; k += 4) {
+      const float4 v = part[(int64_t)k * (D / 4)];
+      const float w = s_w[k];
+      s4.x = fmaf(v.x, w, s4.x);
+      s4.y = fmaf(v.y, w, s4.y);
+      s4.z = fmaf(v.z, w, s4.z);
+      s4.w = fmaf(v.w, w, s4.w);
+    }
+    reinterpret_cast<float4*>(s_red[kg])[dq] = s4;
+  }
+  __syncthreads();
+  const float num = fmaf(acc, s_fin[0], s_red[0][d] + s_red[1][d] + s_red[2][d] + s_red[3][d]);
+  const float den = s_fin[1];
+  a.out[((int64_t)b * Hq + j) * D + d] = den > 0.f ? num / den : 0.f;
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -684,22 +885,32 @@ int launch_decode_hq2b(const AttnArgs& a_in, cudaStream_t stream) {
   AttnArgs a = a_in;
   if (a.lanes > MAX_LANES_FAST) return KVQ_ERR_UNSUPPORTED;
   const int grid = sm_count() * DEC_CTAS_PER_SM;
-  a.grid_warps = grid * DEC_WARPS;
+  a.grid_warps = grid * DEC_PAIRS;     // work is split over warp pairs
   a.min_wp = decode_hq2b_min_wp(a.max_seq_len);
-  const size_t smem = (size_t)DEC_WARPS * DEC_STAGES * STAGE_BYTES + DEC_WARPS * DEC_STAGES * 8 +
-                      (size_t)(a.lanes + 1) * sizeof(int);
+  const size_t fixed = (size_t)DEC_PAIRS * PAIR_BYTES + DEC_PAIRS * PB_COUNT * 8;
+  const size_t smem = fixed + (size_t)(a.lanes + 1) * sizeof(int);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
-    cudaFuncSetAttribute(decode_hq2b_main<DEC_STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         DEC_WARPS * DEC_STAGES * STAGE_BYTES + DEC_WARPS * DEC_STAGES * 8 +
-                             (MAX_LANES_FAST + 1) * (int)sizeof(int));
+    cudaFuncSetAttribute(decode_hq2b_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)(fixed + (MAX_LANES_FAST + 1) * sizeof(int)));
     attr_set[dev] = true;
   }
-  decode_hq2b_main<DEC_STAGES><<<grid, DEC_WARPS * 32, smem, stream>>>(a);
-  decode_hq2b_combine<<<dim3(a.lanes, a.c.num_q_heads), 256, 0, stream>>>(a);
+  decode_hq2b_main<<<grid, DEC_PAIRS * 64, smem, stream>>>(a);
+  // the combine may start while the main grid drains; it waits for it before reading partials
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.lanes, a.c.num_q_heads);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_hq2b_combine, a) != cudaSuccess) return KVQ_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

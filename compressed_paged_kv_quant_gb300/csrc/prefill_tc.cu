@@ -13,14 +13,14 @@
 //                        S/P double buffer [128,192) [192,256): S lands in fp32, P is written
 //                        back over its first 32 columns as fp16 pairs (A operand of O += P V);
 //                        O [256,512) fp32 accumulator of the split.
-//   Shared memory:       K tile x2 (64 keys x 256 dims fp16, 128B-swizzled K-major = B of S),
-//                        V^T tile x2 (256 dims x 64 keys fp16, 128B-swizzled K-major = B of PV),
+//   Shared memory:       K tile x2 (64 keys x 256 dims fp16, 128B-swizzled, K-major B of S),
+//                        V tile x2 (the same [key][dim] layout, read as the MN-major B of PV),
 //                        compressed-page staging x2 (one 9,216 B TMA bulk copy per page).
 //   Warps 0-3: softmax, one row per thread (= TMEM lane): S from TMEM, causal mask, online
 //              max with lazy O rescale (only when a row max grows by more than 2^8), P to
 //              TMEM, l in FP32; the epilogue writes (m, l, O) of the split.
-//   Warps 4-7: page TMA (one elected thread) and dequantisation into the swizzled tiles.
-//   Warp 8:    one thread issues every tcgen05.mma (S(j+1) ahead of PV(j)) and commits
+//   Warps 4-10: page TMA (one elected thread) and dequantisation into the swizzled tiles.
+//   Warp 11:   one thread issues every tcgen05.mma (S(j+1) ahead of PV(j)) and commits
 //              their completion to mbarriers.
 // Every mbarrier wait is bounded; on a timeout the CTA flags KVQ_STATUS_TIMEOUT, stops, waits
 // (bounded) for its copies and MMAs in flight, and still releases its TMEM.
@@ -30,7 +30,9 @@
 namespace kvq {
 
 constexpr int PT_ROWS = 128;
-constexpr int PT_THREADS = 9 * 32;
+constexpr int PT_DQ_WARPS = 7;                    // TMA + dequantisation warps (12 warps: <= 168 regs)
+constexpr int PT_MMA_WARP = 4 + PT_DQ_WARPS;      // the warp whose lane 0 issues the MMAs
+constexpr int PT_THREADS = (PT_MMA_WARP + 1) * 32;
 constexpr int PT_STAGE = 2 * HQ2B_BLOCK;  // compressed K + V block of one page (one layer/head)
 constexpr int SM_K = 0;                   // 2 x 32 KB
 constexpr int SM_V = 65536;               // 2 x 32 KB
@@ -119,9 +121,21 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-// instruction descriptor: D f32, A f16, B f16, both K-major, M x N
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// shared-memory matrix descriptor: 128B swizzle, MN-major (the N index runs along the 128 B rows):
+// 64-element N blocks `lbo` bytes apart, 8-row K groups `sbo` bytes apart
+constexpr uint32_t PV_LBO = 8192, PV_SBO = 1024;
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(PV_LBO >> 4) << 16;
+  d |= (uint64_t)(PV_SBO >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// instruction descriptor: D f32, A f16, B f16, A K-major, B K-major (or MN-major), M x N
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false) {
+  return (1u << 4) | (b_mn_major ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // byte offset of 16 B chunk `chunk` (0..7) of `row` in a 128B-swizzled region (1,024 B atoms)
@@ -129,8 +143,40 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk) {
   return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+__device__ __forceinline__ float ex2f(float x) {  // 2^x, one MUFU.EX2
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t h2u(__half2 x) { return *reinterpret_cast<uint32_t*>(&x); }
 __device__ __forceinline__ __half2 u2h(uint32_t x) { return *reinterpret_cast<__half2*>(&x); }
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u8 %0, [%1];\n" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+// Two code bytes (dims 4k + j of byte k at bits 2j) -> four fp16 pairs holding 4 + c for dims
+// (0,1), (2,3), (4,5), (6,7): each multiply spreads a byte to two places (no overlap, so it is an
+// OR), the mask keeps one code per half at mantissa bits 8-9, the exponent of 4 makes it 4 + c.
+__device__ __forceinline__ void dq_pairs(uint32_t lo, uint32_t hi, uint32_t (&x)[4]) {
+  x[0] = ((lo * 0x00400100u) & 0x03000300u) | 0x44004400u;
+  x[1] = ((lo * 0x00040010u) & 0x03000300u) | 0x44004400u;
+  x[2] = ((hi * 0x00400100u) & 0x03000300u) | 0x44004400u;
+  x[3] = ((hi * 0x00040010u) & 0x03000300u) | 0x44004400u;
+}
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -175,10 +221,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; i++) {
       bar_init(BAR(B_STG_FULL + i), 1);
-      bar_init(BAR(B_STG_EMPTY + i), 4);
-      bar_init(BAR(B_K_FULL + i), 4);
+      bar_init(BAR(B_STG_EMPTY + i), PT_DQ_WARPS);
+      bar_init(BAR(B_K_FULL + i), PT_DQ_WARPS);
       bar_init(BAR(B_K_EMPTY + i), 1);
-      bar_init(BAR(B_V_FULL + i), 4);
+      bar_init(BAR(B_V_FULL + i), PT_DQ_WARPS);
       bar_init(BAR(B_S_FULL + i), 1);
       bar_init(BAR(B_P_FULL + i), 4);
       bar_init(BAR(B_PV_DONE + i), 1);
@@ -241,13 +287,22 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       TC_LD32(tl + TM_S0 + 64 * buf + 32, (sv + 32));
       tc_wait_ld();
       const int key0 = (p0 + j) * P;
+      // a tile entirely below the causal diagonal of every row of the CTA needs no mask (rows
+      // past the last query hold Q = 0 and are never written)
+      const bool full = key0 + P - 1 <= qpos0 + q_first;
       float tmax = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int cidx = 0; cidx < 64; cidx++) {
-        const bool ok = row_valid && key0 + cidx <= qpos;
-        const float x = ok ? __uint_as_float(sv[cidx]) * a.scale_log2 : -INFINITY;
-        sv[cidx] = __float_as_uint(x);
-        tmax = fmaxf(tmax, x);
+        for (int cidx = 0; cidx < 64; cidx++) tmax = fmaxf(tmax, __uint_as_float(sv[cidx]));
+        tmax *= a.scale_log2;
+      } else {
+#pragma unroll
+        for (int cidx = 0; cidx < 64; cidx++) {
+          const bool ok = row_valid && key0 + cidx <= qpos;
+          const float x = ok ? __uint_as_float(sv[cidx]) * a.scale_log2 : -INFINITY;
+          sv[cidx] = __float_as_uint(x);
+          tmax = fmaxf(tmax, x);
+        }
       }
       const float m_new = fmaxf(m_run, tmax);
       const bool first = (j == 0) || (m_run == -INFINITY);
@@ -259,7 +314,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
           break;
         }
         tc_fence_after();
-        const float alpha = need ? exp2f(m_run - m_new) : 1.0f;
+        const float alpha = need ? ex2f(m_run - m_new) : 1.0f;
         for (int ch = 0; ch < 8; ch++) {
           uint32_t o[32];
           TC_LD32(tl + TM_O + 32 * ch, o);
@@ -278,13 +333,24 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       uint32_t pr[32];
       float psum = 0.f;
+      if (full) {
+        const float sc = a.scale_log2, nm = -m_use;
 #pragma unroll
-      for (int i = 0; i < 32; i++) {
-        const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
-        const float e0 = x0 == -INFINITY ? 0.f : exp2f(x0 - m_use);
-        const float e1 = x1 == -INFINITY ? 0.f : exp2f(x1 - m_use);
-        psum += e0 + e1;
-        pr[i] = h2u(__floats2half2_rn(e0, e1));
+        for (int i = 0; i < 32; i++) {
+          const float e0 = ex2f(fmaf(__uint_as_float(sv[2 * i]), sc, nm));
+          const float e1 = ex2f(fmaf(__uint_as_float(sv[2 * i + 1]), sc, nm));
+          psum += e0 + e1;
+          pr[i] = h2u(__floats2half2_rn(e0, e1));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+          const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
+          const float e0 = ex2f(x0 - m_use);   // 2^-inf = 0 for masked keys
+          const float e1 = ex2f(x1 - m_use);
+          psum += e0 + e1;
+          pr[i] = h2u(__floats2half2_rn(e0, e1));
+        }
       }
       l_run += psum;
       TC_ST32(tl + TM_S0 + 64 * buf, pr);
@@ -315,9 +381,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       }
       if (row_valid) reinterpret_cast<float2*>(a.ws_ml)[pidx] = make_float2(m_run, l_run);
     }
-  } else if (warp < 8) {
+  } else if (warp < PT_MMA_WARP) {
     // =============================================================== TMA + dequant warps
-    const int tid = threadIdx.x - 128;
+    const int tid = threadIdx.x - 128;             // 0 .. 32 * PT_DQ_WARPS - 1
+    constexpr int DQ_T = 32 * PT_DQ_WARPS;
     const int64_t lane_row = (int64_t)b * c.max_pages;
     auto issue = [&](int j) -> bool {
       const int buf = j & 1;
@@ -346,81 +413,70 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
         if (!issue(issued)) { timed_out = true; break; }
     }
     const __half2 two = __float2half2_rn(2.0f), m11 = __float2half2_rn(-11.0f);
+    const __half2 one2 = __float2half2_rn(1.0f), m4 = __float2half2_rn(-4.0f);
+    // Item = (key t, chunk cc = dims 8cc .. 8cc+7); DQ_T is a multiple of 32, so a thread keeps
+    // its chunk for the whole tile and walks keys t0, t0 + KSTEP, ...  Both tiles are stored
+    // [dim block cc/8][key t][chunk cc%8 ^ t%8]: a warp writes one key row, 512 contiguous
+    // bytes of swizzled chunks, free of bank conflicts.
+    const int cc = tid & 31, t0 = tid >> 5;
+    constexpr int KSTEP = DQ_T / 32;
+    const uint32_t tile_off = (uint32_t)(cc >> 3) * 8192u;
     for (int j = 0; j < ntiles && !timed_out; j++) {
       const int buf = j & 1;
       const uint32_t par = (j >> 1) & 1;
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) { timed_out = true; break; }
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_STG_FULL + buf), par))) { timed_out = true; break; }
-      const uint8_t* stg = smem + SM_STG + buf * PT_STAGE;
+      const uint32_t stg = sm_u32(smem + SM_STG + buf * PT_STAGE);
       const int key0 = (p0 + j) * P;
-      // ---- K tile (B of S): element (key t, dim d) at atom d/64, row t, chunk (d%64)/8
+      // ---- K tile (B of S, K-major): k^ = s_d (2c - 3)
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_K_EMPTY + buf), par ^ 1))) { timed_out = true; break; }
-      const uint32_t kb = sm_u32(smem + SM_K + buf * 32768);
-#pragma unroll 4
-      for (int i = 0; i < 16; i++) {
-        const int item = tid + 128 * i;
-        const int t = item >> 5, cc = item & 31;
-        const int kp = key0 + t;
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (kp < len) {
-          if (kp >= ef) {
-            const uint4 w =
-                reinterpret_cast<const uint4*>(c.ring + ((((int64_t)b * c.num_layers + c.layer) * H + h) * P + (kp % P)) * D)[cc];
-            o.x = h2u(__floats2half2_rn(bf16_lo(w.x), bf16_hi(w.x)));
-            o.y = h2u(__floats2half2_rn(bf16_lo(w.y), bf16_hi(w.y)));
-            o.z = h2u(__floats2half2_rn(bf16_lo(w.z), bf16_hi(w.z)));
-            o.w = h2u(__floats2half2_rn(bf16_lo(w.w), bf16_hi(w.w)));
-          } else {
-            const uint32_t w16 = *reinterpret_cast<const uint16_t*>(stg + t * HQ2B_ROW + 2 * cc);
-            const uint4 sc = *reinterpret_cast<const uint4*>(stg + HQ2B_META_OFF + 16 * cc);
-            // byte k of the code word holds dims 8cc + 4k .. +3; spread each byte so that codes
-            // (2p, 2p+1) of the chunk land in mantissa bits 8-9 of the two halves
-            const uint32_t lo = w16 & 0xFFu, hi = w16 >> 8;
-            const uint32_t ua = (lo << 8) | (lo << 22), ub = (hi << 8) | (hi << 22);
-            const uint32_t spread[4] = {ua, ua >> 4, ub, ub >> 4};
-            const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
-            uint32_t res[4];
+      const uint32_t kb = sm_u32(smem + SM_K + buf * 32768) + tile_off;
+      {
+        const uint4 sc = ld_shared_v4(stg + HQ2B_META_OFF + 16 * cc);
+        const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
+#pragma unroll 2
+        for (int t = t0; t < P; t += KSTEP) {
+          const int kp = key0 + t;
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          if (kp < len) {
+            if (kp >= ef) {
+              const uint4 w = reinterpret_cast<const uint4*>(
+                  c.ring + ((((int64_t)b * c.num_layers + c.layer) * H + h) * P + (kp % P)) * D)[cc];
+              o.x = h2u(__floats2half2_rn(bf16_lo(w.x), bf16_hi(w.x)));
+              o.y = h2u(__floats2half2_rn(bf16_lo(w.y), bf16_hi(w.y)));
+              o.z = h2u(__floats2half2_rn(bf16_lo(w.z), bf16_hi(w.z)));
+              o.w = h2u(__floats2half2_rn(bf16_lo(w.w), bf16_hi(w.w)));
+            } else {
+              uint32_t res[4];
+              dq_pairs(ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc), ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1), res);
 #pragma unroll
-            for (int p = 0; p < 4; p++) {
-              const uint32_t x = (spread[p] & 0x03000300u) | 0x44004400u;        // (4 + c) pairs
-              const __half2 y = __hfma2(u2h(x), two, m11);                        // 2c - 3, exact
-              res[p] = h2u(__hmul2(y, u2h(scs[p])));                              // s_d (2c - 3)
+              for (int p = 0; p < 4; p++) res[p] = h2u(__hmul2(__hfma2(u2h(res[p]), two, m11), u2h(scs[p])));
+              o = make_uint4(res[0], res[1], res[2], res[3]);
             }
-            o = make_uint4(res[0], res[1], res[2], res[3]);
           }
+          st_shared_v4(kb + swz(t, cc & 7), o);
         }
-        st_shared_v4(kb + (cc >> 3) * 8192 + swz(t, cc & 7), o);
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       __syncwarp();
       if (lane == 0) bar_arrive(BAR(B_K_FULL + buf));
-      // ---- V^T tile (B of PV): element (dim d, key t) at row d, chunk t/8
+      // ---- V tile (B of PV, MN-major): v^ = z + c s, one rounding, per token and 128-dim half
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_PV_DONE + buf), par ^ 1))) { timed_out = true; break; }
-      const uint32_t vb = sm_u32(smem + SM_V + buf * 32768);
-      const uint8_t* vst = stg + HQ2B_BLOCK;
-#pragma unroll 1
-      for (int i = 0; i < 4; i++) {
-        const int item = tid + 128 * i;   // 512 items: byte column q x key chunk kc
-        const int q = item & 63, kc = item >> 6;
-        const int hf = q >> 5;
-        float v[4][8];
+      const uint32_t vb = sm_u32(smem + SM_V + buf * 32768) + tile_off;
+      const uint32_t vst = stg + HQ2B_BLOCK;
+#pragma unroll 2
+      for (int t = t0; t < P; t += KSTEP) {
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (key0 + t < len) {
+          const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+          const __half2 s2 = u2h(__byte_perm(meta, 0u, 0x1010u)), z2 = u2h(__byte_perm(meta, 0u, 0x3232u));
+          uint32_t res[4];
+          dq_pairs(ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc), ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1), res);
 #pragma unroll
-        for (int e = 0; e < 8; e++) {
-          const int t = 8 * kc + e;
-          const uint32_t byte = vst[t * HQ2B_ROW + q];
-          const uint32_t meta = *reinterpret_cast<const uint32_t*>(vst + HQ2B_META_OFF + t * 8 + 4 * hf);
-          const float sv = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
-          const float zv = half_bits_to_float((uint16_t)(meta >> 16));
-          const bool ok = key0 + t < len;
-#pragma unroll
-          for (int k = 0; k < 4; k++) v[k][e] = ok ? fmaf((float)((byte >> (2 * k)) & 3u), sv, zv) : 0.f;
+          for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
+          o = make_uint4(res[0], res[1], res[2], res[3]);
         }
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const uint4 o = make_uint4(h2u(__floats2half2_rn(v[k][0], v[k][1])), h2u(__floats2half2_rn(v[k][2], v[k][3])),
-                                     h2u(__floats2half2_rn(v[k][4], v[k][5])), h2u(__floats2half2_rn(v[k][6], v[k][7])));
-          st_shared_v4(vb + swz(4 * q + k, kc), o);
-        }
+        st_shared_v4(vb + swz(t, cc & 7), o);
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       __syncwarp();
@@ -442,7 +498,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
     // =============================================================== MMA warp (one thread)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = idesc_f16(128, 64);
-      constexpr uint32_t IDESC_PV = idesc_f16(128, 256);
+      constexpr uint32_t IDESC_PV = idesc_f16(128, 256, true);
       bool ok = bar_wait(BAR(B_Q_READY), 0);
       tc_fence_after();
       auto issue_s = [&](int j) -> bool {
@@ -470,7 +526,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
         const uint32_t vb = sm_u32(smem + SM_V + buf * 32768);
 #pragma unroll
         for (int ks = 0; ks < 4; ks++)
-          tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_desc(vb + 32 * ks), IDESC_PV,
+          tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_mn_desc(vb + 2048 * ks), IDESC_PV,
                     (j > 0 || ks > 0) ? 1u : 0u);
         tc_commit(BAR(B_PV_DONE + buf));
         last_pv = j;
