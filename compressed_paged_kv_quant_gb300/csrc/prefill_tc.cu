@@ -44,6 +44,7 @@ constexpr int SM_TMEM = SM_ABORT + 4;
 constexpr int PT_SMEM = SM_TMEM + 12 + 1024;  // + slack to align the base to 1,024 B
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr int PT_SPIN = 1 << 16;
+constexpr int PT_POLL = 1 << 22;   // MMA-issuer polls (20 ns sleep each): ~0.1 s before giving up
 constexpr float RESCALE_LOG2 = 8.0f;
 
 enum {
@@ -58,6 +59,15 @@ __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void bar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
   for (int i = 0; i < PT_SPIN; i++) {
@@ -290,20 +300,25 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       // a tile entirely below the causal diagonal of every row of the CTA needs no mask (rows
       // past the last query hold Q = 0 and are never written)
       const bool full = key0 + P - 1 <= qpos0 + q_first;
-      float tmax = -INFINITY;
+      // row max and (below) row sum as 8 independent chains: the softmax sits between S and
+      // P.V on the tensor pipe, so its latency, not its instruction count, is what matters
+      float t8[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) t8[i] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int cidx = 0; cidx < 64; cidx++) tmax = fmaxf(tmax, __uint_as_float(sv[cidx]));
-        tmax *= a.scale_log2;
+        for (int cidx = 0; cidx < 64; cidx++) t8[cidx & 7] = fmaxf(t8[cidx & 7], __uint_as_float(sv[cidx]));
       } else {
 #pragma unroll
         for (int cidx = 0; cidx < 64; cidx++) {
           const bool ok = row_valid && key0 + cidx <= qpos;
           const float x = ok ? __uint_as_float(sv[cidx]) * a.scale_log2 : -INFINITY;
           sv[cidx] = __float_as_uint(x);
-          tmax = fmaxf(tmax, x);
+          t8[cidx & 7] = fmaxf(t8[cidx & 7], x);
         }
       }
+      float tmax = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+      if (full) tmax *= a.scale_log2;
       const float m_new = fmaxf(m_run, tmax);
       const bool first = (j == 0) || (m_run == -INFINITY);
       const bool need = !first && (m_new > m_run + RESCALE_LOG2);
@@ -332,14 +347,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       if (first) m_run = m_new;
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       uint32_t pr[32];
-      float psum = 0.f;
+      float ps[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) ps[i] = 0.f;
       if (full) {
         const float sc = a.scale_log2, nm = -m_use;
 #pragma unroll
         for (int i = 0; i < 32; i++) {
           const float e0 = ex2f(fmaf(__uint_as_float(sv[2 * i]), sc, nm));
           const float e1 = ex2f(fmaf(__uint_as_float(sv[2 * i + 1]), sc, nm));
-          psum += e0 + e1;
+          ps[i & 7] += e0 + e1;
           pr[i] = h2u(__floats2half2_rn(e0, e1));
         }
       } else {
@@ -348,11 +365,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
           const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
           const float e0 = ex2f(x0 - m_use);   // 2^-inf = 0 for masked keys
           const float e1 = ex2f(x1 - m_use);
-          psum += e0 + e1;
+          ps[i & 7] += e0 + e1;
           pr[i] = h2u(__floats2half2_rn(e0, e1));
         }
       }
-      l_run += psum;
+      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       TC_ST32(tl + TM_S0 + 64 * buf, pr);
       tc_wait_st();
       tc_fence_before();
@@ -434,6 +451,16 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       {
         const uint4 sc = ld_shared_v4(stg + HQ2B_META_OFF + 16 * cc);
         const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
+        if (key0 + P <= ef) {   // every key of the tile comes from the codes (ef <= len)
+#pragma unroll 2
+          for (int t = t0; t < P; t += KSTEP) {
+            uint32_t res[4];
+            dq_pairs(ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc), ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1), res);
+#pragma unroll
+            for (int p = 0; p < 4; p++) res[p] = h2u(__hmul2(__hfma2(u2h(res[p]), two, m11), u2h(scs[p])));
+            st_shared_v4(kb + swz(t, cc & 7), make_uint4(res[0], res[1], res[2], res[3]));
+          }
+        } else
 #pragma unroll 2
         for (int t = t0; t < P; t += KSTEP) {
           const int kp = key0 + t;
@@ -464,10 +491,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_PV_DONE + buf), par ^ 1))) { timed_out = true; break; }
       const uint32_t vb = sm_u32(smem + SM_V + buf * 32768) + tile_off;
       const uint32_t vst = stg + HQ2B_BLOCK;
+      const bool vall = key0 + P <= len;
 #pragma unroll 2
       for (int t = t0; t < P; t += KSTEP) {
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (key0 + t < len) {
+        if (vall || key0 + t < len) {
           const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
           const __half2 s2 = u2h(__byte_perm(meta, 0u, 0x1010u)), z2 = u2h(__byte_perm(meta, 0u, 0x3232u));
           uint32_t res[4];
@@ -501,9 +529,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       constexpr uint32_t IDESC_PV = idesc_f16(128, 256, true);
       bool ok = bar_wait(BAR(B_Q_READY), 0);
       tc_fence_after();
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j) {
         const int buf = j & 1;
-        if (!bar_wait(BAR(B_K_FULL + buf), (j >> 1) & 1)) return false;
         tc_fence_after();
         const uint32_t kb = sm_u32(smem + SM_K + buf * 32768);
 #pragma unroll
@@ -512,16 +539,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
                     IDESC_S, ks > 0);
         tc_commit(BAR(B_S_FULL + buf));
         tc_commit(BAR(B_K_EMPTY + buf));
-        return true;
       };
-      int last_pv = -1;
-      if (ok && ntiles > 0) ok = issue_s(0);
-      for (int j = 0; j < ntiles && ok; j++) {
-        if (*abort_flag) { ok = false; break; }
-        if (j + 1 < ntiles && !issue_s(j + 1)) { ok = false; break; }
+      auto issue_pv = [&](int j) {
         const int buf = j & 1;
-        const uint32_t par = (j >> 1) & 1;
-        if (!bar_wait(BAR(B_P_FULL + buf), par) || !bar_wait(BAR(B_V_FULL + buf), par)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vb = sm_u32(smem + SM_V + buf * 32768);
 #pragma unroll
@@ -529,7 +549,36 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
           tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_mn_desc(vb + 2048 * ks), IDESC_PV,
                     (j > 0 || ks > 0) ? 1u : 0u);
         tc_commit(BAR(B_PV_DONE + buf));
-        last_pv = j;
+      };
+      int last_pv = -1;
+      if (ok && ntiles > 0) {
+        ok = bar_wait(BAR(B_K_FULL), 0);
+        if (ok) issue_s(0);
+      }
+      // Per tile j: S(j+1) once its K tile is ready and PV(j) once P(j) and the V tile are;
+      // whichever is ready first goes first (S(j+1) preferred), so a late dequant does not hold
+      // back PV(j) and a late softmax does not hold back S(j+1).  S(j+1) reuses the S/P buffer of
+      // tile j-1, whose PV was issued in the previous round.
+      for (int j = 0; j < ntiles && ok; j++) {
+        if (*abort_flag) { ok = false; break; }
+        const int buf = j & 1;
+        const uint32_t par = (j >> 1) & 1;
+        bool s_done = j + 1 >= ntiles, pv_done = false;
+        for (int spin = 0; !(s_done && pv_done); spin++) {
+          if (spin > PT_POLL) { ok = false; break; }
+          if (!s_done && bar_test(BAR(B_K_FULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) {
+            issue_s(j + 1);
+            s_done = true;
+            continue;
+          }
+          if (!pv_done && bar_test(BAR(B_P_FULL + buf), par) && bar_test(BAR(B_V_FULL + buf), par)) {
+            issue_pv(j);
+            last_pv = j;
+            pv_done = true;
+            continue;
+          }
+          __nanosleep(20);
+        }
       }
       if (!ok) {
         timed_out = true;
