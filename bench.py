@@ -43,6 +43,34 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+DECODE_SOURCES = ("decode_hq2b.cu", "kvq_internal.cuh", "attn_args.cuh", "append_ops.cuh")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_hq2b_main_27b_8x40960.md")
+
+
+def _decode_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "compressed_paged_kv_quant_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _decode_traffic():
+    """DRAM bytes per decode_hq2b_main launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (its `traffic:` line records both); else None."""
+    try:
+        with open(DECODE_PROFILE) as f:
+            for line in f:
+                if line.startswith("traffic:"):
+                    fields = dict(kv.split("=", 1) for kv in line[len("traffic:"):].split())
+                    if fields.get("source_sha256") == _decode_source_hash():
+                        return int(fields["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
 def _config(extra=None):
     c = {"workload": "decode_27b_8x40960: 16 layers x 4 KV heads x 256, 24 q heads, 8 lanes x 40,960 tokens, "
                      "2-bit pages (72 B/head/token), append + decode per layer",
@@ -232,8 +260,11 @@ def run_gpu(args):
 
     def step():
         for l in range(L):
-            dw.append_step(l, k_v[l], v_v[l])
-            dw.decode(l, q_v[l], ws, step_out[l])
+            if args.step_calls == "fused":
+                dw.decode_step(l, q_v[l], k_v[l], v_v[l], ws, step_out[l])
+            else:
+                dw.append_step(l, k_v[l], v_v[l])
+                dw.decode(l, q_v[l], ws, step_out[l])
 
     # capture one step in a CUDA graph
     with torch.cuda.stream(stream):
@@ -336,9 +367,10 @@ def run_gpu(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (2-bit codes)", "data": "synthetic",
-                "config": _config({"ms_per_attention_call": call_ms, "peak_source": peak_src}),
+                "config": _config({"ms_per_attention_call": call_ms, "peak_source": peak_src,
+                                   "step_calls": args.step_calls}),
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                             "frac": achieved / peak, "traffic": None,
+                             "frac": achieved / peak, "traffic": _decode_traffic(),
                              "kernel": "paged_decode_attn (decode_hq2b_main + decode_hq2b_combine), one layer",
                              "algorithmic_bytes_per_launch": attn_bytes},
                 "cpu_baseline": cpu,
@@ -441,6 +473,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],
+                    help="one kvq_decode_step per layer, or kv_quant_append + paged_decode_attn")
     ap.add_argument("--prefill-prefix", type=int, default=65536)
     ap.add_argument("--prefill-steps", type=int, default=3)
     args = ap.parse_args()

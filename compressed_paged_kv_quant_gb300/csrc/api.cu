@@ -95,6 +95,29 @@ int check_attn_common(const kvq_geom* g, int layer, const void* pool, size_t poo
   return KVQ_OK;
 }
 
+AttnArgs decode_args(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring, int window,
+                     const int32_t* page_table, int max_pages, int lanes, const int32_t* seq_len, int max_seq_len,
+                     const void* q, float sm_scale, void* workspace, float* out, int32_t* d_status) {
+  AttnArgs a{};
+  a.c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, window, d_status);
+  a.q_pos0 = a.n_q = a.q_offset = nullptr;
+  a.seq_len = seq_len;
+  a.lanes = lanes;
+  a.max_n_q = 1;
+  a.n_q_rows = lanes;
+  a.split_tokens = decode_split_tokens(g->format);
+  a.max_splits = (int)decode_slots(g->format, max_seq_len);
+  a.grid_warps = 0;
+  a.min_wp = 0;
+  a.max_seq_len = max_seq_len;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.scale_log2 = sm_scale * LOG2E;
+  a.ws_o = static_cast<float*>(workspace);
+  a.ws_ml = a.ws_o + (int64_t)lanes * g->num_q_heads * a.max_splits * D;
+  a.out = out;
+  return a;
+}
+
 }  // namespace
 
 extern "C" {
@@ -167,23 +190,8 @@ int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t poo
                              max_seq_len, q, workspace, out, d_status);
   if (rc || lanes == 0) return rc;
   if (ws_bytes < kvq_decode_workspace_bytes(g, lanes, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-  AttnArgs a;
-  a.c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, window, d_status);
-  a.q_pos0 = a.n_q = a.q_offset = nullptr;
-  a.seq_len = seq_len;
-  a.lanes = lanes;
-  a.max_n_q = 1;
-  a.n_q_rows = lanes;
-  a.split_tokens = decode_split_tokens(g->format);
-  a.max_splits = (int)decode_slots(g->format, max_seq_len);
-  a.grid_warps = 0;
-  a.min_wp = 0;
-  a.max_seq_len = max_seq_len;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.scale_log2 = sm_scale * LOG2E;
-  a.ws_o = static_cast<float*>(workspace);
-  a.ws_ml = a.ws_o + (int64_t)lanes * g->num_q_heads * a.max_splits * D;
-  a.out = out;
+  AttnArgs a = decode_args(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
+                           max_seq_len, q, sm_scale, workspace, out, d_status);
   if (g->format == KVQ_FMT_HQ2B) return launch_decode_hq2b(a, (cudaStream_t)stream);
   return launch_attn_generic(g->format, a, 1, (cudaStream_t)stream);
 }
@@ -200,7 +208,7 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
   if (lanes == 0 || max_n_q == 0) return KVQ_OK;
   if (!q_pos0 || !n_q || !q_offset) return KVQ_ERR_INVALID_ARG;
   if (ws_bytes < kvq_prefill_workspace_bytes(g, n_q_rows, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-  AttnArgs a;
+  AttnArgs a{};
   a.c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, window, d_status);
   a.q_pos0 = q_pos0;
   a.n_q = n_q;
@@ -224,6 +232,38 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
     return rc ? rc : launch_attn_combine(a, 0, (cudaStream_t)stream);
   }
   return launch_attn_generic(g->format, a, 0, (cudaStream_t)stream);
+}
+
+int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes, void* ring, int window,
+                    const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
+                    const int32_t* n_new, const int32_t* tok_offset, int n_rows, const void* k, const void* v,
+                    const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale, void* workspace,
+                    size_t ws_bytes, float* out, int32_t* d_status, kvq_stream_t stream) {
+  int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
+                             max_seq_len, q, workspace, out, d_status);
+  if (rc) return rc;
+  if (n_rows < 0) return KVQ_ERR_INVALID_ARG;
+  if (lanes == 0) return KVQ_OK;
+  if (!start_pos || !n_new || !tok_offset || !k || !v) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
+  if (ws_bytes < kvq_decode_workspace_bytes(g, lanes, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
+  // the append first: a one-launch decode append (at most one token per lane)
+  rc = kv_quant_append(g, layer, pool, pool_bytes, ring, page_table, max_pages, lanes, start_pos, n_new, tok_offset,
+                       1, n_rows, k, v, d_status, stream);
+  if (rc) return rc;
+  if (g->format != KVQ_FMT_HQ2B || lanes > 8192)   // BF16 pages or very many lanes: plain decode after it
+    return paged_decode_attn(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
+                             max_seq_len, q, sm_scale, workspace, ws_bytes, out, d_status, stream);
+  AttnArgs a = decode_args(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
+                           max_seq_len, q, sm_scale, workspace, out, d_status);
+  a.step.start_pos = start_pos;
+  a.step.n_new = n_new;
+  a.step.tok_offset = tok_offset;
+  a.step.n_rows = n_rows;
+  a.step.k = static_cast<const __nv_bfloat16*>(k);
+  a.step.v = static_cast<const __nv_bfloat16*>(v);
+  a.step.active = 1;
+  return launch_decode_hq2b(a, (cudaStream_t)stream);
 }
 
 }  // extern "C"

@@ -4,6 +4,18 @@
 
 namespace kvq {
 
+// The append of a fused decode step (kvq_decode_step), which the decode kernels overlap: at
+// most one new token per lane, at position start_pos[b] == seq_len[b] - 1.
+struct StepAppend {
+  const int32_t* start_pos;
+  const int32_t* n_new;
+  const int32_t* tok_offset;
+  int n_rows;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  int active;
+};
+
 struct AttnArgs {
   CacheView c;
   const int32_t* q_pos0;    // prefill only
@@ -19,6 +31,7 @@ struct AttnArgs {
   int grid_warps;    // fast 2-bit decode: warps of the persistent grid
   int min_wp;        // fast 2-bit decode: least pages per warp (bounds the partials per lane/head)
   int max_seq_len;   // host bound on every seq_len[b]
+  StepAppend step;   // fused decode step only (active == 0 otherwise)
 };
 
 // Resolve query i of lane b: its row, position, and key count.  Returns false (after

@@ -30,6 +30,7 @@
 //     and the "+4" are added back with sum(P z) (FP32) and one all-ones MMA per k-step.
 #include "kvq_internal.cuh"
 #include "attn_args.cuh"
+#include "append_ops.cuh"
 
 namespace kvq {
 
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
   uint4* qsm = reinterpret_cast<uint4*>(pbase + 4 * HQ2B_BLOCK + 2 * X_BYTES);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DEC_PAIRS * PAIR_BYTES) + pair * PB_COUNT;
   int* pre = reinterpret_cast<int*>(smem + DEC_PAIRS * PAIR_BYTES + DEC_PAIRS * PB_COUNT * 8);
+
   auto BAR = [&](int i) { return smem_u32(&bars[i]); };
   // the combine kernel may be scheduled now: it does its own tail work first and waits for
   // this grid's completion before it reads any partial
@@ -235,7 +237,15 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
         const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
         if (lane >= o) incl += t;
       }
-      if (b < a.lanes) pre[b + 1] = carry + incl;
+      if (b < a.lanes) {
+        pre[b + 1] = carry + incl;
+        int cp = -1;
+        if (a.step.active && a.step.n_new[b] == 1) {
+          const int st = a.step.start_pos[b];
+          if (st >= 0 && (st + 1) % P == 0) cp = st / P;
+        }
+        pre[a.lanes + 1 + b] = cp;   // fused decode step: the page the step's token closes, or -1
+      }
       carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
     if (lane == 0) pre[0] = 0;
@@ -255,7 +265,10 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
   const int gp = blockIdx.x * DEC_PAIRS + pair;
   const int u0 = gp * Wp;
   const int u1 = min(u0 + Wp, units);
-  if (u0 >= u1) return;
+  if (u0 >= u1) {
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");   // see the end of the kernel
+    return;
+  }
   const int n_units = u1 - u0;
 
   Cursor cu;
@@ -272,6 +285,9 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
     int32_t phys;
     const bool ok = page_phys(c, pc, phys);
     if (ok) {
+      // fused decode step: a page that the step's token closes (a main page only with window 0)
+      // gets its K block and last V row from the append kernel this grid overlaps: wait for it
+      if (a.step.active && pre[a.lanes + 1 + pc.b] == pc.p) asm volatile("griddepcontrol.wait;\n" ::: "memory");
       if (lane == 0) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, pc.h, kv);
@@ -581,6 +597,9 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
   // copies still in flight into this warp's ring must land before the CTA's smem is released
   for (int q = max(0, produced - 2); q < produced; q++)
     if (valid & (1u << (q & 1))) mbar_wait(BAR(full_bar + (q & 1)), (q >> 1) & 1u);
+  // in a fused decode step this grid completes only after the append it overlaps, so the
+  // combine kernel's wait for this grid covers the append as well (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
 }
 
 // ----------------------------------------------------------------------------- combine + tail
@@ -591,7 +610,7 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
 // partials of this (lane, head) with the tail in FP32.
 constexpr int TAIL_MAX = 2 * P;   // len - tail_start < 2 pages, since the window is at most a page
 
-__global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
+__global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
   const int b = blockIdx.x, j = blockIdx.y, h = j / G;
@@ -627,6 +646,25 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
   const int ef = bad ? 0 : exact_from(len, c.window);
   const int tail_start = npg * P;
   const int ntail = bad ? 0 : len - tail_start;
+  // fused decode step: this step's token (position len - 1) may still be being appended while
+  // this part runs, so the tail takes its key and value from the step inputs, never from the
+  // ring or the page
+  int st_start = 0, st_n = 0, st_off = 0;
+  if (a.step.active && !bad) {
+    st_start = a.step.start_pos[b];
+    st_n = a.step.n_new[b];
+    st_off = a.step.tok_offset[b];
+    if (st_n < 0 || st_n > 1 || st_start < 0 || st_off < 0 || st_off + st_n > a.step.n_rows ||
+        (st_n == 1 && st_start != len - 1) || (st_n == 0 && st_start != len)) {
+      if (tid == 0 && j % G == 0) flag(c.status, KVQ_STATUS_BAD_LEN);
+      st_n = 0;
+    }
+  }
+  const int t_new = st_n ? st_start - tail_start : -1;   // tail index of the step token, or -1
+  // the tail reads K codes of a page this step closes only for 0 < window < 64 (the close then
+  // leaves keys below exact_from in that page): then wait for the step's append to be complete
+  // (the main grid waits for it before it exits)
+  if (st_n == 1 && (st_start + 1) % P == 0 && tail_start < ef) asm volatile("griddepcontrol.wait;\n" ::: "memory");
   if (tid < 2) {
     const int p = tail_start / P + tid;
     int32_t phys = -1;
@@ -651,6 +689,7 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
   // ---- part 1a: tail V rows to shared memory (64 B codes + 8 B meta each)
   for (int i = tid; i < ntail * 4; i += blockDim.x) {
     const int t = i >> 2, pos = tail_start + t;
+    if (t == t_new) continue;
     const int32_t phys = s_phys[pos / P - tail_start / P];
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
     if (phys >= 0) {
@@ -665,6 +704,13 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
       s_vm[t][0] = s_vm[t][1] = 0u;
     }
     reinterpret_cast<uint4*>(s_vc[t])[i & 3] = w;
+  }
+  if (t_new >= 0 && warp == 0) {       // the step token's V row, quantized exactly as the append does
+    const uint4 vx = reinterpret_cast<const uint4*>(a.step.v + ((int64_t)st_off * H + h) * D)[lane];
+    uint32_t packed, meta;
+    quant_v_row(vx, packed, meta);
+    reinterpret_cast<uint16_t*>(s_vc[t_new])[lane] = (uint16_t)packed;
+    if ((lane & 15) == 0) s_vm[t_new][lane >> 4] = meta;
   }
   // ---- part 1b: tail scores; warp w takes keys w, w + 8, ..., four at a time, lanes over dims
   float q[8];
@@ -702,7 +748,9 @@ __global__ void __launch_bounds__(256) decode_hq2b_combine(AttnArgs a) {
       const int t = t0 + 8 * u, pos = tail_start + t;
       kw[u] = make_uint4(0u, 0u, 0u, 0u);
       if (t < ntail) {
-        if (pos >= ef)
+        if (t == t_new && pos >= ef)   // (below exact_from it is read from the codes, like any key)
+          kw[u] = reinterpret_cast<const uint4*>(a.step.k + ((int64_t)st_off * H + h) * D)[lane];
+        else if (pos >= ef)
           kw[u] = reinterpret_cast<const uint4*>(c.ring + ring_row_offset(c, b, h, pos % P))[lane];
         else if (kblk0)
           kw[u].x = reinterpret_cast<const uint16_t*>(kblk0 + (pos % P) * HQ2B_ROW)[lane];
@@ -888,17 +936,32 @@ int launch_decode_hq2b(const AttnArgs& a_in, cudaStream_t stream) {
   a.grid_warps = grid * DEC_PAIRS;     // work is split over warp pairs
   a.min_wp = decode_hq2b_min_wp(a.max_seq_len);
   const size_t fixed = (size_t)DEC_PAIRS * PAIR_BYTES + DEC_PAIRS * PB_COUNT * 8;
-  const size_t smem = fixed + (size_t)(a.lanes + 1) * sizeof(int);
+  const size_t smem = fixed + (size_t)(2 * a.lanes + 1) * sizeof(int);
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
     cudaFuncSetAttribute(decode_hq2b_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)(fixed + (MAX_LANES_FAST + 1) * sizeof(int)));
+                         (int)(fixed + (2 * MAX_LANES_FAST + 1) * sizeof(int)));
     attr_set[dev] = true;
   }
-  decode_hq2b_main<<<grid, DEC_PAIRS * 64, smem, stream>>>(a);
+  if (a.step.active) {
+    // fused decode step: overlap the append kernel launched just before
+    cudaLaunchConfig_t mc = {};
+    mc.gridDim = dim3(grid);
+    mc.blockDim = dim3(DEC_PAIRS * 64);
+    mc.dynamicSmemBytes = smem;
+    mc.stream = stream;
+    cudaLaunchAttribute mattr[1];
+    mattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    mattr[0].val.programmaticStreamSerializationAllowed = 1;
+    mc.attrs = mattr;
+    mc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&mc, decode_hq2b_main, a) != cudaSuccess) return KVQ_ERR_CUDA;
+  } else {
+    decode_hq2b_main<<<grid, DEC_PAIRS * 64, smem, stream>>>(a);
+  }
   // the combine may start while the main grid drains; it waits for it before reading partials
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.lanes, a.c.num_q_heads);

@@ -35,7 +35,7 @@ STATUS_TIMEOUT = 16
 EXPORTS = ("kvq_page_bytes", "kvq_token_bytes", "kvq_ring_bytes", "kvq_pool_pages",
            "kvq_decode_workspace_bytes", "kvq_prefill_workspace_bytes", "kvq_strerror",
            "kvq_build_arch", "kv_quant_append", "paged_decode_attn", "paged_prefill_attn",
-           "paged_decode_attn_noalloc")
+           "paged_decode_attn_noalloc", "kvq_decode_step")
 
 
 class KvqError(RuntimeError):
@@ -100,6 +100,9 @@ def lib():
             L.paged_prefill_attn.restype = i32
             L.paged_decode_attn_noalloc.argtypes = [G, i32, P, sz, P, i32, P, i32, i32, P, i32, P, f32, P, P, P]
             L.paged_decode_attn_noalloc.restype = i32
+            L.kvq_decode_step.argtypes = [G, i32, P, sz, P, i32, P, i32, i32, P, P, P, i32, P, P, P, i32, P, f32, P,
+                                          sz, P, P, P]
+            L.kvq_decode_step.restype = i32
             _lib = L
     return _lib
 
@@ -192,6 +195,20 @@ def paged_decode_attn_noalloc(g: Geom, layer: int, pool, ring, window: int, page
                                          _ptr(page_table), page_table.shape[1], n_lanes, _ptr(seq_len), max_seq_len,
                                          _ptr(q), float(sm_scale), _ptr(out), _ptr(status), _stream(stream))
     _check(rc, "paged_decode_attn_noalloc")
+
+
+def kvq_decode_step(g: Geom, layer: int, pool, ring, window: int, page_table, start_pos, n_new, tok_offset, k, v,
+                    seq_len, max_seq_len: int, q, sm_scale: float, workspace, out, status, stream=None,
+                    n_rows: Optional[int] = None):
+    """Append at most one token per lane, then decode attention over the cache that includes it
+    (see ``kvq_decode_step`` in kvq.h)."""
+    lanes, max_pages = page_table.shape[0], page_table.shape[1]
+    rows = k.shape[0] if n_rows is None else n_rows
+    rc = lib().kvq_decode_step(ctypes.byref(g), layer, _ptr(pool), _nbytes(pool), _ptr(ring), window,
+                               _ptr(page_table), max_pages, lanes, _ptr(start_pos), _ptr(n_new), _ptr(tok_offset),
+                               rows, _ptr(k), _ptr(v), _ptr(seq_len), max_seq_len, _ptr(q), float(sm_scale),
+                               _ptr(workspace), _nbytes(workspace), _ptr(out), _ptr(status), _stream(stream))
+    _check(rc, "kvq_decode_step")
 
 
 def paged_prefill_attn(g: Geom, layer: int, pool, ring, window: int, page_table, q_pos0, n_q,

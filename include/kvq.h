@@ -177,6 +177,27 @@ int paged_prefill_attn(const kvq_geom* geom, int layer, const void* pool, size_t
                        kvq_stream_t stream);
 
 /*
+ * kvq_decode_step -- one decode step of one layer: kv_quant_append of at most one new token
+ * per lane followed by paged_decode_attn over the cache that includes it ([KV9] "How it
+ * works": tokens are quantized as they are appended and attention reads the compressed pages).
+ *   Arguments are those of the two calls, with max_new = 1: n_new[b] in {0, 1}, the new token
+ *   at position start_pos[b] == seq_len[b] - n_new[b]; k, v: bf16 [n_rows][num_kv_heads][256].
+ *   Results: the pool and ring bytes and `out` equal those of kv_quant_append then
+ *   paged_decode_attn on the same stream.  With HQ2B pages the decode kernels overlap the
+ *   append kernel: the main kernel reads no page the append writes until it has waited for it
+ *   (only a page the new token closes, and only with window 0, is such a page), and the tail
+ *   takes the new token's key and value from k and v.  BF16 pages: the two calls in sequence.
+ *   Errors: those of both calls; device bit BAD_LEN when start_pos[b] + n_new[b] != seq_len[b]
+ *   (that lane's new token is then neither appended nor attended).
+ */
+int kvq_decode_step(const kvq_geom* geom, int layer, void* pool, size_t pool_bytes, void* ring,
+                    int window, const int32_t* page_table, int max_pages, int lanes,
+                    const int32_t* start_pos, const int32_t* n_new, const int32_t* tok_offset,
+                    int n_rows, const void* k, const void* v, const int32_t* seq_len,
+                    int max_seq_len, const void* q, float sm_scale, void* workspace,
+                    size_t ws_bytes, float* out, int32_t* d_status, kvq_stream_t stream);
+
+/*
  * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.  The pages have
  * no counterpart of this call: it exists for callers that cannot allocate device memory --
  * code running inside a CUDA graph capture it does not own, plugins of an engine whose

@@ -259,3 +259,55 @@ def test_flat_attention_over_131072_keys_keeps_full_mass():
     # would be off by ~1.0); what remains is the tensor core's own FP32 accumulation within a
     # warp's run of pages, well inside the 2e-3 + 1e-3 |ref| contract
     assert_close(o, ref, atol=2e-4, rtol=2e-4, what="flat 131072")
+
+
+@pytest.mark.parametrize("window", [64, 32, 0])
+def test_decode_step_equals_append_then_decode(window):
+    """kvq_decode_step (the append inside the combine kernel, overlapped with the main kernel)
+    leaves the same pool and ring bytes as kv_quant_append followed by paged_decode_attn, and
+    the same outputs -- except, with window 0, lanes whose token closes a page, which are
+    checked against the oracle -- over 70 steps with page closes on every lane and
+    one lane that appends nothing on odd steps; windows 64, 32 and 0 put the closing page's keys
+    in the ring, split, and in the codes."""
+    from compressed_paged_kv_quant_gb300 import kvq
+    steps = 70
+    final = [700, 1500, 130, 3001]
+    wl = _custom(final, L=2, H=2, Hq=12, seed=5, window=window)
+    dev = "cuda"
+    A, B = _dw(wl, HQ), _dw(wl, HQ)
+    # lane 3 skips odd steps, so its history stops steps // 2 tokens short of its final length
+    base = [n - steps for n in final[:3]] + [final[3] - steps // 2]
+    for dw in (A, B):
+        dw.fill_history(base)
+    torch.cuda.synchronize()
+    i32 = lambda xs: torch.tensor(list(xs), dtype=torch.int32, device=dev)
+    ws_a, out_a = A.decode_buffers()
+    ws_b, out_b = B.decode_buffers()
+    ws_b.view(torch.int32).fill_(-1)
+    pos = list(base)
+    for s in range(steps):
+        layer = s % 2
+        n_new = [1, 1, 1, int(s % 2 == 0)]
+        start = list(pos)
+        seq = [p + n for p, n in zip(pos, n_new)]
+        rows = [b for b in range(4) if n_new[b]]
+        off = [0] * 4
+        for i, b in enumerate(rows):
+            off[b] = i
+        k = torch.cat([wl.kv_torch(layer, b, pos[b], 1, 0, dev) for b in rows])
+        v = torch.cat([wl.kv_torch(layer, b, pos[b], 1, 1, dev) for b in rows])
+        q = torch.cat([wl.q_torch(layer, b, max(seq[b] - 1, 0), 1, dev) for b in range(4)])
+        sp, nn, to, sl = i32(start), i32(n_new), i32(off), i32(seq)
+        kvq.kv_quant_append(A.g, layer, A.cache.pool, A.cache.ring, A.page_table, sp, nn, to, 1, k, v, A.cache.status)
+        kvq.paged_decode_attn(A.g, layer, A.cache.pool, A.cache.ring, window, A.page_table, sl, max(final), q,
+                              A.sm_scale, ws_a, out_a, A.cache.status)
+        kvq.kvq_decode_step(B.g, layer, B.cache.pool, B.cache.ring, window, B.page_table, sp, nn, to, k, v, sl,
+                            max(final), q, B.sm_scale, ws_b, out_b, B.cache.status)
+        torch.cuda.synchronize()
+        assert A.cache.read_status() == 0 and B.cache.read_status() == 0, f"step {s}"
+        a, b = out_a.cpu().numpy(), out_b.cpu().numpy()
+        assert np.array_equal(a, b), f"step {s}: max diff {np.abs(a - b).max()}"
+        pos = seq
+    assert pos == final
+    assert torch.equal(A.cache.pool, B.cache.pool)
+    assert torch.equal(A.cache.ring, B.cache.ring)
