@@ -353,6 +353,7 @@ def run_gpu(args):
         e2e_ms = float(t.item())
     e2e_value = world * tokens_per_step / (e2e_ms / 1000.0)
 
+    moves = None if args.no_page_moves else run_page_moves(dw, stream)
     prefill = None if args.no_prefill else run_prefill(args, dev, stream)
 
     cpu = None
@@ -377,11 +378,53 @@ def run_gpu(args):
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": 3 * L * args.steps,
                 "clocks": clk,
-                "prefill": prefill}
+                "prefill": prefill,
+                "page_moves": moves}
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def run_page_moves(dw, stream, reps=5):
+    """Bit-exact page moves of one lane's whole context (640 pages of the 27B geometry, every layer
+    and head, 377 MB): gather to a pinned host arena, scatter back, and gather to a device arena;
+    next to one contiguous cudaMemcpyAsync of the same bytes each way (the copy engines)."""
+    import torch
+
+    from compressed_paged_kv_quant_gb300 import kvq
+    ids = torch.from_numpy(dw.wl.page_table[0][dw.wl.page_table[0] >= 0].copy()).to(dw.device)
+    pb = kvq.page_bytes(dw.g)
+    nbytes = ids.numel() * pb
+    host = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    devbuf = torch.empty(nbytes, dtype=torch.uint8, device=dw.device)
+
+    def timed(fn):
+        ts = []
+        with torch.cuda.stream(stream):
+            fn()
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                stream.synchronize()
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    st = stream.cuda_stream
+    g_h = timed(lambda: kvq.pages_gather(dw.g, dw.cache.pool, ids, host, dw.cache.status, st))
+    s_h = timed(lambda: kvq.pages_scatter(dw.g, dw.cache.pool, ids, host, dw.cache.status, st))
+    g_d = timed(lambda: kvq.pages_gather(dw.g, dw.cache.pool, ids, devbuf, dw.cache.status, st))
+    c_dh = timed(lambda: host.copy_(devbuf, non_blocking=True))
+    c_hd = timed(lambda: devbuf.copy_(host, non_blocking=True))
+    assert dw.cache.read_status() == 0, "device status flagged during page moves"
+    gbs = lambda ms, factor=1: factor * nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"{ids.numel()} pages x {pb} B (one lane, all layers and heads)", "bytes": nbytes,
+            "gather_to_pinned_host_gbs": gbs(g_h), "scatter_from_pinned_host_gbs": gbs(s_h),
+            "gather_device_to_device_gbs": gbs(g_d, 2),
+            "memcpy_device_to_host_gbs": gbs(c_dh), "memcpy_host_to_device_gbs": gbs(c_hd),
+            "note": "device-to-device counts read + write bytes; host legs count the bytes moved"}
 
 
 def prefill_flops(prefix, chunk, q_heads):
@@ -473,6 +516,7 @@ def main():
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-page-moves", action="store_true")
     ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],
                     help="one kvq_decode_step per layer, or kv_quant_append + paged_decode_attn")
     ap.add_argument("--prefill-prefix", type=int, default=65536)

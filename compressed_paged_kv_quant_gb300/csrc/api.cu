@@ -17,6 +17,8 @@ int prefill_split_tokens(int fmt);
 int decode_hq2b_slots(int max_seq_len);
 int launch_prefill_hq2b_tc(const AttnArgs& a, cudaStream_t stream);
 int launch_attn_combine(const AttnArgs& a, int decode, cudaStream_t stream);
+int launch_page_move(uint8_t* pool, uint8_t* arena, const int32_t* page_ids, int n_pages, int64_t page_bytes,
+                     int64_t pool_pages, int gather, int32_t* status, cudaStream_t stream);
 }  // namespace kvq
 
 #include "attn_args.cuh"
@@ -264,6 +266,30 @@ int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes,
   a.step.v = static_cast<const __nv_bfloat16*>(v);
   a.step.active = 1;
   return launch_decode_hq2b(a, (cudaStream_t)stream);
+}
+
+static int page_move(const kvq_geom* g, void* pool, size_t pool_bytes, const int32_t* page_ids, int n_pages,
+                     void* arena, int gather, int32_t* d_status, kvq_stream_t stream) {
+  int rc = check_geom(g);
+  if (rc) return rc;
+  if (n_pages < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_pages == 0) return KVQ_OK;
+  if (!pool || !page_ids || !arena || !d_status) return KVQ_ERR_INVALID_ARG;
+  if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(pool) || !aligned16(arena)) return KVQ_ERR_ALIGNMENT;
+  const int64_t pb = (int64_t)page_bytes_of(g);
+  return launch_page_move(static_cast<uint8_t*>(pool), static_cast<uint8_t*>(arena), page_ids, n_pages, pb,
+                          (int64_t)(pool_bytes / pb), gather, d_status, (cudaStream_t)stream);
+}
+
+int kvq_pages_gather(const kvq_geom* g, const void* pool, size_t pool_bytes, const int32_t* page_ids, int n_pages,
+                     void* arena, int32_t* d_status, kvq_stream_t stream) {
+  return page_move(g, const_cast<void*>(pool), pool_bytes, page_ids, n_pages, arena, 1, d_status, stream);
+}
+
+int kvq_pages_scatter(const kvq_geom* g, void* pool, size_t pool_bytes, const int32_t* page_ids, int n_pages,
+                      const void* arena, int32_t* d_status, kvq_stream_t stream) {
+  return page_move(g, pool, pool_bytes, page_ids, n_pages, const_cast<void*>(arena), 0, d_status, stream);
 }
 
 }  // extern "C"

@@ -35,7 +35,7 @@ STATUS_TIMEOUT = 16
 EXPORTS = ("kvq_page_bytes", "kvq_token_bytes", "kvq_ring_bytes", "kvq_pool_pages",
            "kvq_decode_workspace_bytes", "kvq_prefill_workspace_bytes", "kvq_strerror",
            "kvq_build_arch", "kv_quant_append", "paged_decode_attn", "paged_prefill_attn",
-           "paged_decode_attn_noalloc", "kvq_decode_step")
+           "paged_decode_attn_noalloc", "kvq_decode_step", "kvq_pages_gather", "kvq_pages_scatter")
 
 
 class KvqError(RuntimeError):
@@ -103,6 +103,10 @@ def lib():
             L.kvq_decode_step.argtypes = [G, i32, P, sz, P, i32, P, i32, i32, P, P, P, i32, P, P, P, i32, P, f32, P,
                                           sz, P, P, P]
             L.kvq_decode_step.restype = i32
+            L.kvq_pages_gather.argtypes = [G, P, sz, P, i32, P, P, P]
+            L.kvq_pages_gather.restype = i32
+            L.kvq_pages_scatter.argtypes = [G, P, sz, P, i32, P, P, P]
+            L.kvq_pages_scatter.restype = i32
             _lib = L
     return _lib
 
@@ -157,6 +161,13 @@ def _check(rc: int, what: str):
         raise KvqError(rc, what)
 
 
+def _arena_ptr(t) -> int:
+    """A page arena: a contiguous CUDA tensor, or pinned host memory (under unified addressing the
+    host pointer of pinned memory is valid on the device)."""
+    assert t.is_contiguous() and (t.is_cuda or t.is_pinned()), "the arena must be a CUDA or pinned host tensor"
+    return t.data_ptr()
+
+
 def _nbytes(t) -> int:
     return t.numel() * t.element_size()
 
@@ -209,6 +220,20 @@ def kvq_decode_step(g: Geom, layer: int, pool, ring, window: int, page_table, st
                                rows, _ptr(k), _ptr(v), _ptr(seq_len), max_seq_len, _ptr(q), float(sm_scale),
                                _ptr(workspace), _nbytes(workspace), _ptr(out), _ptr(status), _stream(stream))
     _check(rc, "kvq_decode_step")
+
+
+def pages_gather(g: Geom, pool, page_ids, arena, status, stream=None):
+    """Copy pool pages page_ids[i] into arena slot i (see ``kvq_pages_gather`` in kvq.h)."""
+    rc = lib().kvq_pages_gather(ctypes.byref(g), _ptr(pool), _nbytes(pool), _ptr(page_ids), page_ids.numel(),
+                                _arena_ptr(arena), _ptr(status), _stream(stream))
+    _check(rc, "kvq_pages_gather")
+
+
+def pages_scatter(g: Geom, pool, page_ids, arena, status, stream=None):
+    """Copy arena slot i into pool page page_ids[i] (see ``kvq_pages_scatter`` in kvq.h)."""
+    rc = lib().kvq_pages_scatter(ctypes.byref(g), _ptr(pool), _nbytes(pool), _ptr(page_ids), page_ids.numel(),
+                                 _arena_ptr(arena), _ptr(status), _stream(stream))
+    _check(rc, "kvq_pages_scatter")
 
 
 def paged_prefill_attn(g: Geom, layer: int, pool, ring, window: int, page_table, q_pos0, n_q,

@@ -198,6 +198,27 @@ int kvq_decode_step(const kvq_geom* geom, int layer, void* pool, size_t pool_byt
                     size_t ws_bytes, float* out, int32_t* d_status, kvq_stream_t stream);
 
 /*
+ * kvq_pages_gather / kvq_pages_scatter -- bit-exact page moves between the pool and an arena
+ * ([REUSE] "What a sequence is made of": pages are the unit a cache evicts to a slower tier
+ * and brings back).
+ *   gather:  arena slot i (page_bytes each, slot i at arena + i * kvq_page_bytes(geom)) <-
+ *            pool page page_ids[i], for i < n_pages.
+ *   scatter: pool page page_ids[i] <- arena slot i.
+ *   A page is moved as opaque bytes -- every layer and head, codes, scales and metadata -- so
+ *   scattering gathered pages to other page ids and pointing the page table at them leaves
+ *   every attention result bit for bit the same.  The exact-key ring is per lane, not per
+ *   page, and is not moved.  arena: device memory or pinned host memory the GPU can address
+ *   (on a Grace host the kernel reads and writes it directly over NVLink-C2C); 16-byte
+ *   aligned.  page_ids: device int32 [n_pages]; ids repeated in one scatter race.
+ *   Errors: KVQ_ERR_INVALID_ARG / UNSUPPORTED / ALIGNMENT / CUDA; device bit PAGE_OOB (that
+ *   page is not moved).
+ */
+int kvq_pages_gather(const kvq_geom* geom, const void* pool, size_t pool_bytes, const int32_t* page_ids,
+                     int n_pages, void* arena, int32_t* d_status, kvq_stream_t stream);
+int kvq_pages_scatter(const kvq_geom* geom, void* pool, size_t pool_bytes, const int32_t* page_ids,
+                      int n_pages, const void* arena, int32_t* d_status, kvq_stream_t stream);
+
+/*
  * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.  The pages have
  * no counterpart of this call: it exists for callers that cannot allocate device memory --
  * code running inside a CUDA graph capture it does not own, plugins of an engine whose

@@ -213,3 +213,33 @@ def prefill(g: Geom, layer: int, pool, ring, window: int, page_table, lanes: int
                            pt.shape[1], lanes, K(q_pos0, np.int32), K(n_q, np.int32),
                            K(q_offset, np.int32), K(seq_len, np.int32), K(qa), sm_scale, K(out))
     return out, int(st)
+
+
+def pages_gather(g: Geom, pool: np.ndarray, page_ids) -> np.ndarray:
+    """Page moves ("The KV cache and prompt reuse", "What a sequence is made of": whole pages are
+    what a cache moves to a slower tier and back): arena slot i holds the bytes of pool page
+    page_ids[i].  A page is opaque bytes; ids outside the pool are skipped (slot left zero) and
+    reported as PAGE_OOB."""
+    pb = page_bytes(g)
+    n_pool = pool.size // pb
+    arena = np.zeros(len(page_ids) * pb, np.uint8)
+    st = 0
+    for i, p in enumerate(page_ids):
+        if 0 <= p < n_pool:
+            arena[i * pb:(i + 1) * pb] = pool[p * pb:(p + 1) * pb]
+        else:
+            st |= PAGE_OOB
+    return arena, st
+
+
+def pages_scatter(g: Geom, pool: np.ndarray, page_ids, arena: np.ndarray) -> int:
+    """Inverse move: pool page page_ids[i] takes the bytes of arena slot i (in place)."""
+    pb = page_bytes(g)
+    n_pool = pool.size // pb
+    st = 0
+    for i, p in enumerate(page_ids):
+        if 0 <= p < n_pool:
+            pool[p * pb:(p + 1) * pb] = arena[i * pb:(i + 1) * pb]
+        else:
+            st |= PAGE_OOB
+    return st

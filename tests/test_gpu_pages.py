@@ -1,0 +1,96 @@
+"""Page moves on the GPU: pool pages gathered into a pinned host arena (and a device arena) are
+byte-identical to the oracle's gather of the same pool, and scattering them to other page ids
+with the page table pointed there leaves decode attention bit for bit the same."""
+import numpy as np
+import pytest
+
+import oracle
+from compressed_paged_kv_quant_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from compressed_paged_kv_quant_gb300 import build
+    build.build()
+
+
+def _workload(lens, seed=2):
+    pages = [(n + 63) // 64 for n in lens]
+    total = sum(pages) + 5
+    perm = synth.permutation(seed, total, salt=9)
+    t = np.full((len(lens), max(pages)), -1, np.int32)
+    off = 0
+    for b, p in enumerate(pages):
+        t[b, :p] = perm[off:off + p]
+        off += p
+    return synth.Workload(f"pages_{lens}", 2, 2, 8, list(lens), t, total, window=64, seed=seed)
+
+
+@pytest.mark.parametrize("where", ["host", "device"])
+def test_gather_scatter_moves_pages_bit_exact(where):
+    from compressed_paged_kv_quant_gb300 import kvq
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+    wl = _workload([700, 130, 2000])
+    dw = DeviceWorkload(wl, kvq.FMT_HQ2B, "cuda", fill=0x5A)
+    dw.fill_history(wl.seq_len)
+    torch.cuda.synchronize()
+    g = oracle.geom(oracle.FMT_HQ2B, wl.num_layers, wl.num_kv_heads, wl.num_q_heads)
+    pb = oracle.page_bytes(g)
+    used = sorted({int(p) for p in wl.page_table.ravel() if p >= 0})
+    ids = [used[i] for i in np.random.default_rng(4).permutation(len(used))]
+    ids_t = torch.tensor(ids, dtype=torch.int32, device="cuda")
+    if where == "host":
+        arena = torch.empty(len(ids) * pb, dtype=torch.uint8).pin_memory()
+    else:
+        arena = torch.empty(len(ids) * pb, dtype=torch.uint8, device="cuda")
+    kvq.pages_gather(dw.g, dw.cache.pool, ids_t, arena, dw.cache.status)
+    torch.cuda.synchronize()
+    assert dw.cache.read_status() == 0
+    pool_np = dw.cache.pool.cpu().numpy()
+    ref, st = oracle.pages_gather(g, pool_np, ids)
+    assert st == 0
+    assert np.array_equal(arena.cpu().numpy(), ref)
+
+    # scatter into a second pool at other ids, repoint the page table, decode: same bits
+    new_ids = [(p + 3) % wl.pool_pages for p in ids]
+    remap = dict(zip(ids, new_ids))
+    dw2 = DeviceWorkload(wl, kvq.FMT_HQ2B, "cuda", fill=0x33)
+    dw2.cache.ring.copy_(dw.cache.ring)               # the ring is per lane, not paged
+    kvq.pages_scatter(dw2.g, dw2.cache.pool, torch.tensor(new_ids, dtype=torch.int32, device="cuda"), arena,
+                      dw2.cache.status)
+    pt2 = np.vectorize(lambda p: remap.get(int(p), -1) if p >= 0 else -1)(wl.page_table).astype(np.int32)
+    dw2.page_table = torch.from_numpy(pt2).cuda()
+    torch.cuda.synchronize()
+    assert dw2.cache.read_status() == 0
+    pool2 = dw2.cache.pool.cpu().numpy()
+    for p, q in remap.items():
+        assert np.array_equal(pool2[q * pb:(q + 1) * pb], pool_np[p * pb:(p + 1) * pb])
+    for layer in range(wl.num_layers):
+        q = dw.step_q(layer)
+        ws1, out1 = dw.decode_buffers()
+        ws2, out2 = dw2.decode_buffers()
+        dw.decode(layer, q, ws1, out1)
+        dw2.decode(layer, q, ws2, out2)
+        torch.cuda.synchronize()
+        assert torch.equal(out1, out2)
+    assert dw.cache.read_status() == 0 and dw2.cache.read_status() == 0
+
+
+def test_page_move_flags_bad_id():
+    from compressed_paged_kv_quant_gb300 import kvq
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+    wl = _workload([64])
+    dw = DeviceWorkload(wl, kvq.FMT_HQ2B, "cuda", fill=0x11)
+    pb = kvq.page_bytes(dw.g)
+    arena = torch.full((2 * pb,), 0x77, dtype=torch.uint8, device="cuda")
+    ids = torch.tensor([0, wl.pool_pages], dtype=torch.int32, device="cuda")
+    kvq.pages_gather(dw.g, dw.cache.pool, ids, arena, dw.cache.status)
+    torch.cuda.synchronize()
+    assert dw.cache.read_status() == oracle.PAGE_OOB
+    a = arena.cpu().numpy()
+    assert np.all(a[:pb] == 0x11) and np.all(a[pb:] == 0x77)     # the bad slot is left alone

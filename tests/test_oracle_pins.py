@@ -541,3 +541,26 @@ def test_attend_flags_missing_page():
     bad[0, 1] = -1
     _, _, st = oracle.attend(g, 0, pool, ring, 0, bad[0], 0, 128, 0, np.zeros(256, np.uint16), 100, 0.0625)
     assert st & oracle.PAGE_OOB
+
+
+def test_page_moves_round_trip_and_identity():
+    """Gather then scatter back to the same ids is the identity; scatter to other ids moves each
+    page's bytes unchanged (the pool is opaque bytes per page); a bad id is flagged."""
+    g = oracle.geom(oracle.FMT_HQ2B, 2, 1, 4)
+    pb = oracle.page_bytes(g)
+    assert pb == 2 * 9216
+    rng = np.random.default_rng(3)
+    pool = rng.integers(0, 256, 7 * pb, dtype=np.uint8)
+    ids = [5, 0, 3]
+    arena, st = oracle.pages_gather(g, pool, ids)
+    assert st == 0
+    for i, p in enumerate(ids):
+        assert np.array_equal(arena[i * pb:(i + 1) * pb], pool[p * pb:(p + 1) * pb])
+    back = pool.copy()
+    back[:] = 0
+    assert oracle.pages_scatter(g, back, ids, arena) == 0
+    for p in range(7):
+        want = pool[p * pb:(p + 1) * pb] if p in ids else np.zeros(pb, np.uint8)
+        assert np.array_equal(back[p * pb:(p + 1) * pb], want)
+    _, st = oracle.pages_gather(g, pool, [1, 7])
+    assert st == oracle.PAGE_OOB
