@@ -22,6 +22,7 @@ _lib = None
 
 FMT_HQ2B = 0
 FMT_BF16 = 1
+FMT_HQ2B_HAD = 2   # the 2-bit format over Walsh-Hadamard-rotated K and V rows
 PAGE_OOB, LEN_GT_TABLE, BAD_INPUT, BAD_LEN = 1, 2, 4, 8
 
 
@@ -71,6 +72,10 @@ def lib():
             L.orc_quant_k_page.argtypes = [P, P, P]
             L.orc_dequant_v_row.argtypes = [P, P, P]
             L.orc_dequant_k_row.argtypes = [P, P, P]
+            L.orc_quant_v_row_f32.argtypes = [P, P, P]
+            L.orc_quant_k_page_f32.argtypes = [P, P, P]
+            L.orc_fwht_f32.argtypes = [P]
+            L.orc_hadamard_f64.argtypes = [P, P]
             L.orc_append.argtypes = [G, i32, P, i64, P, P, i32, i32, P, P, P, P, P]
             L.orc_append.restype = i32
             L.orc_attend.argtypes = [G, i32, P, i64, P, i32, P, i32, i32, i32, i32, P, i64, dbl, P, P]
@@ -165,6 +170,24 @@ def dequant_k_row(codes_row, scales) -> np.ndarray:
     out = np.zeros(256, np.float64)
     lib().orc_dequant_k_row(k(codes_row, np.uint8), k(scales, np.uint16), k(out))
     return out
+
+
+def fwht_f32(x: np.ndarray) -> np.ndarray:
+    """The rotated variant's quantizer input: fast Walsh-Hadamard transform of 256 floats in
+    float (stages h = 1..128), then x 1/16."""
+    k = _Keep()
+    y = np.ascontiguousarray(x, dtype=np.float32).copy()
+    assert y.shape == (256,)
+    lib().orc_fwht_f32(k(y))
+    return y
+
+
+def hadamard_f64(x: np.ndarray) -> np.ndarray:
+    """H x in double from the definition H[i][j] = (-1)^popcount(i & j) / 16."""
+    k = _Keep()
+    y = np.zeros(256, np.float64)
+    lib().orc_hadamard_f64(k(x, np.float64), k(y))
+    return y
 
 
 # ------------------------------------------------------------------ cache

@@ -26,6 +26,10 @@
  *     reuse", section "What a sequence is made of").
  *   - attention: softmax(sm_scale * q.k^) weighted sum of v^, in double precision, over the
  *     keys the page table addresses; prefill is causal (a query at position p sees t <= p).
+ *   - rotated variant (format 2): the same 72 B rows over K and V rows rotated by the
+ *     normalized 256-point Walsh-Hadamard transform before quantization (rotation named as
+ *     what makes low-bit caches work in "Half the Cache, Twice the Context"); the ring keeps
+ *     keys unrotated, dequantized page rows are turned back with H (H = H^T = H^-1).
  *   - accumulator model: "Half the Cache, Twice the Context", section "The cliff is in the
  *     accumulator, not the storage" (a running sum rounded after every add; two-level keeps
  *     an FP32 register).
@@ -42,6 +46,7 @@
 #define ORC_P 64
 #define ORC_FMT_HQ2B 0
 #define ORC_FMT_BF16 1
+#define ORC_FMT_HQ2B_HAD 2   /* the 2-bit format over Walsh-Hadamard-rotated K and V rows */
 
 /* status flags (same meaning as the device status word of the GPU library) */
 #define ORC_PAGE_OOB 1
@@ -116,7 +121,7 @@ double orc_kv_bytes_per_token(int layers, int kv_heads, int head_dim, double byt
 
 /* bytes one head's one token costs for K or for V in each format */
 int64_t orc_head_token_bytes(int format) {
-  if (format == ORC_FMT_HQ2B) return 64 + 8;   /* 64 B of 2-bit code + 8 B metadata row */
+  if (format == ORC_FMT_HQ2B || format == ORC_FMT_HQ2B_HAD) return 64 + 8;   /* 64 B code + 8 B meta row */
   if (format == ORC_FMT_BF16) return ORC_D * 2;
   return -1;
 }
@@ -147,14 +152,14 @@ static int input_ok(const uint16_t* x, int n) {
 
 static float clamp03(float r) { return r < 0.0f ? 0.0f : (r > 3.0f ? 3.0f : r); }
 
-/* V: one token row of one head (256 bf16) -> 64 code bytes + meta row [s0, z0, s1, z1]. */
-void orc_quant_v_row(const uint16_t* x, uint8_t* codes, uint16_t* meta) {
+/* V: one token row of one head (256 floats) -> 64 code bytes + meta row [s0, z0, s1, z1]. */
+void orc_quant_v_row_f32(const float* x, uint8_t* codes, uint16_t* meta) {
   memset(codes, 0, 64);
   for (int half = 0; half < 2; half++) {
     int d0 = half * 128;
-    float mn = orc_bf16_to_f32(x[d0]), mx = mn;
+    float mn = x[d0], mx = mn;
     for (int d = d0; d < d0 + 128; d++) {
-      float v = orc_bf16_to_f32(x[d]);
+      float v = x[d];
       if (v < mn) mn = v;
       if (v > mx) mx = v;
     }
@@ -165,7 +170,7 @@ void orc_quant_v_row(const uint16_t* x, uint8_t* codes, uint16_t* meta) {
     for (int d = d0; d < d0 + 128; d++) {
       int c = 0;
       if (sf != 0.0f) {
-        float diff = orc_bf16_to_f32(x[d]) - zf;
+        float diff = x[d] - zf;
         float t = diff / sf;
         c = (int)clamp03(rintf(t));
       }
@@ -176,13 +181,20 @@ void orc_quant_v_row(const uint16_t* x, uint8_t* codes, uint16_t* meta) {
   }
 }
 
-/* K: one closed page of one head (64 rows x 256 bf16) -> 64 x 64 code bytes + 256 scales. */
-void orc_quant_k_page(const uint16_t* x, uint8_t* codes, uint16_t* scales) {
+/* V from bf16 (the plain format): the same steps on the exact float values. */
+void orc_quant_v_row(const uint16_t* x, uint8_t* codes, uint16_t* meta) {
+  float f[ORC_D];
+  for (int d = 0; d < ORC_D; d++) f[d] = orc_bf16_to_f32(x[d]);
+  orc_quant_v_row_f32(f, codes, meta);
+}
+
+/* K: one closed page of one head (64 rows x 256 floats) -> 64 x 64 code bytes + 256 scales. */
+void orc_quant_k_page_f32(const float* x, uint8_t* codes, uint16_t* scales) {
   memset(codes, 0, 64 * 64);
   for (int d = 0; d < ORC_D; d++) {
     float a = 0.0f;
     for (int t = 0; t < ORC_P; t++) {
-      float v = fabsf(orc_bf16_to_f32(x[t * ORC_D + d]));
+      float v = fabsf(x[t * ORC_D + d]);
       if (v > a) a = v;
     }
     uint16_t s = orc_f32_to_f16(a / 3.0f);
@@ -191,7 +203,7 @@ void orc_quant_k_page(const uint16_t* x, uint8_t* codes, uint16_t* scales) {
     for (int t = 0; t < ORC_P; t++) {
       int c = 2;
       if (sf != 0.0f) {
-        float u = orc_bf16_to_f32(x[t * ORC_D + d]) / sf;
+        float u = x[t * ORC_D + d] / sf;
         u = u + 3.0f;
         u = 0.5f * u;
         c = (int)clamp03(rintf(u));
@@ -199,6 +211,46 @@ void orc_quant_k_page(const uint16_t* x, uint8_t* codes, uint16_t* scales) {
       codes[t * 64 + d / 4] |= (uint8_t)(c << (2 * (d % 4)));
     }
   }
+}
+
+/* K from bf16 (the plain format). */
+void orc_quant_k_page(const uint16_t* x, uint8_t* codes, uint16_t* scales) {
+  float* f = (float*)malloc(sizeof(float) * ORC_P * ORC_D);
+  for (int i = 0; i < ORC_P * ORC_D; i++) f[i] = orc_bf16_to_f32(x[i]);
+  orc_quant_k_page_f32(f, codes, scales);
+  free(f);
+}
+
+/* ------------------------------------------------------------------ Hadamard rotation
+ * The rotated variant (a 256-point Walsh-Hadamard transform on K and V before 2-bit
+ * quantization; "Half the Cache, Twice the Context" cites rotation as what makes low-bit
+ * caches work): H = the Sylvester-ordered 256 x 256 Hadamard matrix / 16, so H = H^T = H^-1.
+ * The quantizer's input is defined as the fast transform in float: stages h = 1, 2, 4, ..., 128,
+ * each pair (i, i+h) -> (a + b, a - b) as one IEEE operation each, then x 1/16 (exact). */
+void orc_fwht_f32(float* x) {
+  for (int h = 1; h < ORC_D; h <<= 1)
+    for (int i = 0; i < ORC_D; i += 2 * h)
+      for (int j = i; j < i + h; j++) {
+        float a = x[j], b = x[j + h];
+        x[j] = a + b;
+        x[j + h] = a - b;
+      }
+  for (int i = 0; i < ORC_D; i++) x[i] = x[i] * 0.0625f;
+}
+
+/* H x in double, written from the definition H[i][j] = (-1)^popcount(i & j) / 16. */
+void orc_hadamard_f64(const double* x, double* y) {
+  for (int i = 0; i < ORC_D; i++) {
+    double acc = 0.0;
+    for (int j = 0; j < ORC_D; j++) acc += (__builtin_popcount(i & j) & 1) ? -x[j] : x[j];
+    y[i] = acc / 16.0;
+  }
+}
+
+static int f32_ok(const float* x, int n) {
+  for (int i = 0; i < n; i++)
+    if (!(fabsf(x[i]) <= 65504.0f)) return 0;
+  return 1;
 }
 
 static int code_at(const uint8_t* row, int d) { return (row[d / 4] >> (2 * (d % 4))) & 3; }
@@ -220,7 +272,8 @@ void orc_dequant_k_row(const uint8_t* codes_row, const uint16_t* scales, double*
 
 /* ------------------------------------------------------------------ the paged cache */
 static int geom_ok(const orc_geom* g) {
-  return g && (g->format == ORC_FMT_HQ2B || g->format == ORC_FMT_BF16) && g->head_dim == ORC_D &&
+  return g && (g->format == ORC_FMT_HQ2B || g->format == ORC_FMT_BF16 || g->format == ORC_FMT_HQ2B_HAD) &&
+         g->head_dim == ORC_D &&
          g->page_tokens == ORC_P && g->num_layers > 0 && g->num_kv_heads > 0 &&
          g->num_q_heads > 0 && g->num_q_heads % g->num_kv_heads == 0;
 }
@@ -265,13 +318,41 @@ int orc_append(const orc_geom* g, int layer, uint8_t* pool, int64_t pool_bytes, 
           continue;
         }
         uint16_t meta[4];
-        orc_quant_v_row(vx, vblk + slot * 64, meta);
+        if (g->format == ORC_FMT_HQ2B_HAD) {
+          /* the rotated V row is quantized; the ring keeps the key as it came (exact) */
+          float f[ORC_D];
+          for (int d = 0; d < ORC_D; d++) f[d] = orc_bf16_to_f32(vx[d]);
+          orc_fwht_f32(f);
+          if (!f32_ok(f, ORC_D)) { status |= ORC_BAD_INPUT; continue; }
+          orc_quant_v_row_f32(f, vblk + slot * 64, meta);
+        } else {
+          orc_quant_v_row(vx, vblk + slot * 64, meta);
+        }
         memcpy(vblk + 4096 + slot * 8, meta, 8);
         memcpy(ring_row(ring, g, b, layer, h, slot), kx, ORC_D * 2);
         if (slot == ORC_P - 1) {
           uint16_t scales[ORC_D];
-          orc_quant_k_page(ring_row(ring, g, b, layer, h, 0), kblk, scales);
-          memcpy(kblk + 4096, scales, sizeof scales);
+          if (g->format == ORC_FMT_HQ2B_HAD) {
+            /* the page's 64 keys, each rotated, quantized per channel of the rotated basis */
+            float* f = (float*)malloc(sizeof(float) * ORC_P * ORC_D);
+            const uint16_t* r0 = ring_row(ring, g, b, layer, h, 0);
+            for (int i = 0; i < ORC_P * ORC_D; i++) f[i] = orc_bf16_to_f32(r0[i]);
+            int ok = 1;
+            for (int t2 = 0; t2 < ORC_P; t2++) {
+              orc_fwht_f32(f + t2 * ORC_D);
+              ok = ok && f32_ok(f + t2 * ORC_D, ORC_D);
+            }
+            if (ok) {
+              orc_quant_k_page_f32(f, kblk, scales);
+              memcpy(kblk + 4096, scales, sizeof scales);
+            } else {
+              status |= ORC_BAD_INPUT;
+            }
+            free(f);
+          } else {
+            orc_quant_k_page(ring_row(ring, g, b, layer, h, 0), kblk, scales);
+            memcpy(kblk + 4096, scales, sizeof scales);
+          }
         }
       }
     }
@@ -287,7 +368,7 @@ static int load_key(const orc_geom* g, int layer, const uint8_t* pool, int64_t n
                     int lane, int seq_len, int head, int64_t t, double* out) {
   int64_t open_start = (int64_t)(seq_len / ORC_P) * ORC_P;
   int64_t exact_from = seq_len - window < open_start ? seq_len - window : open_start;
-  if (g->format == ORC_FMT_HQ2B && t >= exact_from) {
+  if (g->format != ORC_FMT_BF16 && t >= exact_from) {
     const uint16_t* r = ring_row((uint16_t*)ring, g, lane, layer, head, (int)(t % ORC_P));
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
     return 0;
@@ -302,6 +383,11 @@ static int load_key(const orc_geom* g, int layer, const uint8_t* pool, int64_t n
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
   } else {
     orc_dequant_k_row(blk + slot * 64, (const uint16_t*)(blk + 4096), out);
+    if (g->format == ORC_FMT_HQ2B_HAD) {   /* the page holds H k: k^ = H (H k)^ */
+      double r[ORC_D];
+      orc_hadamard_f64(out, r);
+      memcpy(out, r, sizeof r);
+    }
   }
   return 0;
 }
@@ -318,6 +404,11 @@ static int load_value(const orc_geom* g, int layer, const uint8_t* pool, int64_t
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
   } else {
     orc_dequant_v_row(blk + slot * 64, (const uint16_t*)(blk + 4096 + slot * 8), out);
+    if (g->format == ORC_FMT_HQ2B_HAD) {   /* the page holds H v: v^ = H (H v)^ */
+      double r[ORC_D];
+      orc_hadamard_f64(out, r);
+      memcpy(out, r, sizeof r);
+    }
   }
   return 0;
 }

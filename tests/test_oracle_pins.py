@@ -564,3 +564,63 @@ def test_page_moves_round_trip_and_identity():
         assert np.array_equal(back[p * pb:(p + 1) * pb], want)
     _, st = oracle.pages_gather(g, pool, [1, 7])
     assert st == oracle.PAGE_OOB
+
+
+def test_hadamard_rotation_matches_scipy_and_is_orthonormal():
+    """The rotated variant's transform: the fast float transform and the double definition both
+    equal scipy's Sylvester Hadamard matrix / 16 applied to x; H H = I; dot products survive."""
+    from scipy.linalg import hadamard
+    H = hadamard(256).astype(np.float64) / 16.0
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(256).astype(np.float32)
+    ref = H @ x.astype(np.float64)
+    assert np.allclose(oracle.hadamard_f64(x.astype(np.float64)), ref, atol=1e-12)
+    assert np.allclose(oracle.fwht_f32(x), ref, rtol=0, atol=2e-6 * np.abs(x).max() * 16)
+    y = oracle.hadamard_f64(oracle.hadamard_f64(x.astype(np.float64)))
+    assert np.allclose(y, x, atol=1e-12)
+    e = np.zeros(256)
+    e[5] = 1.0
+    assert np.array_equal(np.abs(oracle.hadamard_f64(e)), np.full(256, 1.0 / 16))
+    q = rng.standard_normal(256)
+    assert abs(q @ x - oracle.hadamard_f64(q) @ oracle.hadamard_f64(x.astype(np.float64))) < 1e-9
+
+
+def test_rotated_format_attention_matches_unrotated_brute_force():
+    """A tiny rotated-format cache: the oracle's attention equals brute force over keys and
+    values dequantized from the codes and turned back with scipy's Hadamard matrix (one full
+    page plus an open page read from the ring)."""
+    from scipy.linalg import hadamard
+    H = hadamard(256).astype(np.float64) / 16.0
+    g = oracle.geom(oracle.FMT_HQ2B_HAD, 1, 1, 2)
+    pb = oracle.page_bytes(g)
+    n = 100
+    rng = np.random.default_rng(5)
+    kf = (rng.standard_normal((n, 256)) * np.where(np.arange(256) % 16 == 0, 4, 1)).astype(np.float32)
+    vf = rng.standard_normal((n, 256)).astype(np.float32)
+    bf = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)       # truncation is fine for inputs
+    k, v = bf(kf), bf(vf)
+    pool = np.zeros(3 * pb, np.uint8)
+    ring = np.zeros((1, 1, 1, 64, 256), np.uint16)
+    pt = np.array([[2, 0]], np.int32)
+    assert oracle.append(g, 0, pool, ring, pt, 1, [0], [n], [0], k, v) == 0
+    q = bf(rng.standard_normal((1, 2, 256)).astype(np.float32))
+    out, st = oracle.decode(g, 0, pool, ring, 0, pt, 1, np.array([n], np.int32), q, 0.0625)
+    assert st == 0
+    f = lambda u: (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    keys, vals = np.zeros((n, 256)), np.zeros((n, 256))
+    kb = pool[2 * pb:2 * pb + 4608]
+    vb = pool[2 * pb + 4608:2 * pb + 9216]
+    scales = kb[4096:].view(np.uint16)
+    for t in range(n):
+        if t < 64:
+            keys[t] = H @ oracle.dequant_k_row(kb[t * 64:(t + 1) * 64], scales)
+        else:
+            keys[t] = f(k[t])                                            # the open page: ring, exact
+        blk = vb if t < 64 else pool[0 * pb + 4608:0 * pb + 9216]
+        s = t % 64
+        vals[t] = H @ oracle.dequant_v_row(blk[s * 64:(s + 1) * 64], blk[4096 + s * 8:4096 + s * 8 + 8].view(np.uint16))
+    for j in range(2):
+        sc = 0.0625 * (keys @ f(q[0, j]))
+        w = np.exp(sc - sc.max())
+        ref = (w @ vals) / w.sum()
+        assert np.allclose(out[0, j], ref, atol=1e-10)
