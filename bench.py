@@ -29,6 +29,8 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# page formats by name: the binding's (and the oracle's) format constant
+FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD"}
 WORKLOAD = dict(lanes=8, ctx=40960, layers=16, kv_heads=4, q_heads=24)
 METRIC = "decode attn: compressed-KV tokens/s & achieved HBM GB/s (% of peak); prefill TFLOP/s"
 UNIT = "tokens/s"
@@ -150,7 +152,7 @@ class OracleDecode:
     fp64 attention of all 24 query heads over the lane's 40,960 tokens).  The oracle's cost
     does not depend on the values, so one layer's cache stands in for every layer."""
 
-    def __init__(self, seed=0, threads=None):
+    def __init__(self, seed=0, threads=None, fmt="FMT_HQ2B"):
         import numpy as np
 
         import oracle
@@ -159,7 +161,7 @@ class OracleDecode:
         wl = synth.batched_decode_27b(seed=seed)
         self.wl, self.n = wl, wl.seq_len[0]
         n = self.n
-        self.g = oracle.geom(oracle.FMT_HQ2B, 1, wl.num_kv_heads, wl.num_q_heads)
+        self.g = oracle.geom(getattr(oracle, fmt), 1, wl.num_kv_heads, wl.num_q_heads)
         npg = n // 64
         self.pool = np.zeros(npg * oracle.page_bytes(self.g), np.uint8)
         self.ring = np.zeros((1, 1, wl.num_kv_heads, 64, 256), np.uint16)
@@ -238,7 +240,7 @@ def run_gpu(args):
     H, Hq = wl.num_kv_heads, wl.num_q_heads
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
-        dw = DeviceWorkload(wl, kvq.FMT_HQ2B, dev, fill=None, stream=stream.cuda_stream)
+        dw = DeviceWorkload(wl, getattr(kvq, FORMATS[args.format]), dev, fill=None, stream=stream.cuda_stream)
         dw.fill_history([n - 1 for n in wl.seq_len], chunk=16384)
         # one contiguous input buffer (q, k, v of every layer) and one output buffer per step
         n_q, n_kv = lanes * Hq * 256, lanes * H * 256
@@ -354,11 +356,11 @@ def run_gpu(args):
     e2e_value = world * tokens_per_step / (e2e_ms / 1000.0)
 
     moves = None if args.no_page_moves else run_page_moves(dw, stream)
-    prefill = None if args.no_prefill else run_prefill(args, dev, stream)
+    prefill = None if (args.no_prefill or args.format != "hq2b") else run_prefill(args, dev, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        od = OracleDecode(seed=args.seed)
+        od = OracleDecode(seed=args.seed, fmt=FORMATS[args.format])
         od.run(1)
         dt = od.run(args.cpu_repeats)
         cpu = {"value": od.value(args.cpu_repeats, dt), "unit": UNIT, "cores": od.threads, "kind": "oracle",
@@ -369,14 +371,18 @@ def run_gpu(args):
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (2-bit codes)", "data": "synthetic",
                 "config": _config({"ms_per_attention_call": call_ms, "peak_source": peak_src,
-                                   "step_calls": args.step_calls}),
+                                   "step_calls": args.step_calls, "format": args.format}),
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                             "frac": achieved / peak, "traffic": _decode_traffic(),
-                             "kernel": "paged_decode_attn (decode_hq2b_main + decode_hq2b_combine), one layer",
+                             "frac": achieved / peak,
+                             "traffic": _decode_traffic() if args.format == "hq2b" else None,
+                             "kernel": ("paged_decode_attn (decode_hq2b_main + decode_hq2b_combine), one layer"
+                                        if args.format == "hq2b" else
+                                        "paged_decode_attn (rotate_q_kernel + decode_hq2b_main<centred> + "
+                                        "decode_hq2b_combine), one layer"),
                              "algorithmic_bytes_per_launch": attn_bytes},
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": 3 * L * args.steps,
+                "gpu_launches": (3 if args.format == "hq2b" else 4) * L * args.steps,
                 "clocks": clk,
                 "prefill": prefill,
                 "page_moves": moves}
@@ -515,6 +521,9 @@ def main():
     ap.add_argument("--lanes", type=int, default=WORKLOAD["lanes"])
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
+    ap.add_argument("--format", default="hq2b", choices=sorted(FORMATS),
+                    help="page format: hq2b (the benchmark's) or hq2b_had (Walsh-Hadamard-rotated 2-bit; "
+                         "decode only, no prefill)")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-page-moves", action="store_true")
     ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],

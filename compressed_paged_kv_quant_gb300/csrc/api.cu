@@ -31,7 +31,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 int check_geom(const kvq_geom* g) {
   if (!g) return KVQ_ERR_INVALID_ARG;
-  if (g->format != KVQ_FMT_HQ2B && g->format != KVQ_FMT_BF16) return KVQ_ERR_UNSUPPORTED;
+  if (g->format != KVQ_FMT_HQ2B && g->format != KVQ_FMT_BF16 && g->format != KVQ_FMT_HQ2B_HAD)
+    return KVQ_ERR_UNSUPPORTED;
   if (g->head_dim != D || g->page_tokens != P) return KVQ_ERR_UNSUPPORTED;
   if (g->num_layers <= 0 || g->num_kv_heads <= 0 || g->num_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
   if (g->num_layers > 4096 || g->num_kv_heads > 1024) return KVQ_ERR_UNSUPPORTED;
@@ -41,6 +42,10 @@ int check_geom(const kvq_geom* g) {
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// the byte layout a format uses: the rotated variant keeps HQ2B's
+int layout_fmt(int f) { return f == KVQ_FMT_HQ2B_HAD ? KVQ_FMT_HQ2B : f; }
+bool two_bit(int f) { return layout_fmt(f) == KVQ_FMT_HQ2B; }
 
 size_t page_bytes_of(const kvq_geom* g) {
   return (size_t)g->num_layers * g->num_kv_heads * 2 * (size_t)block_bytes(g->format);
@@ -56,6 +61,7 @@ int64_t splits_for(int64_t max_len, int split) { return max_len <= 0 ? 1 : (max_
 
 // partial records per (lane, query head) the decode kernels may write
 int64_t decode_slots(int fmt, int max_seq_len) {
+  fmt = layout_fmt(fmt);
   return fmt == KVQ_FMT_HQ2B ? decode_hq2b_slots(max_seq_len) : splits_for(max_seq_len, decode_split_tokens(fmt));
 }
 
@@ -75,6 +81,7 @@ CacheView make_view(const kvq_geom* g, int layer, const void* pool, size_t pool_
   c.layer = layer;
   c.window = window;
   c.status = status;
+  c.rotated = g->format == KVQ_FMT_HQ2B_HAD;
   return c;
 }
 
@@ -90,7 +97,7 @@ int check_attn_common(const kvq_geom* g, int layer, const void* pool, size_t poo
   if ((int64_t)max_pages * P > (int64_t)INT32_MAX) return KVQ_ERR_INVALID_ARG;
   if (lanes == 0) return KVQ_OK;
   if (!pool || !page_table || !seq_len || !q || !workspace || !out || !d_status) return KVQ_ERR_INVALID_ARG;
-  if (g->format == KVQ_FMT_HQ2B && !ring) return KVQ_ERR_INVALID_ARG;
+  if (two_bit(g->format) && !ring) return KVQ_ERR_INVALID_ARG;
   if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(pool) || !aligned16(ring) || !aligned16(q) || !aligned16(workspace) || !aligned16(out))
     return KVQ_ERR_ALIGNMENT;
@@ -129,7 +136,7 @@ size_t kvq_page_bytes(const kvq_geom* g) { return check_geom(g) ? 0 : page_bytes
 size_t kvq_token_bytes(const kvq_geom* g) { return check_geom(g) ? 0 : page_bytes_of(g) / P; }
 
 size_t kvq_ring_bytes(const kvq_geom* g, int lanes) {
-  if (check_geom(g) || lanes < 0 || g->format != KVQ_FMT_HQ2B) return 0;
+  if (check_geom(g) || lanes < 0 || !two_bit(g->format)) return 0;
   return (size_t)lanes * g->num_layers * g->num_kv_heads * P * D * 2;
 }
 
@@ -140,7 +147,9 @@ int64_t kvq_pool_pages(const kvq_geom* g, size_t pool_bytes) {
 
 size_t kvq_decode_workspace_bytes(const kvq_geom* g, int lanes, int max_seq_len) {
   if (check_geom(g) || lanes < 0 || max_seq_len < 0) return 0;
-  return partial_bytes(lanes, g->num_q_heads, decode_slots(g->format, max_seq_len));
+  size_t bytes = partial_bytes(lanes, g->num_q_heads, decode_slots(g->format, max_seq_len));
+  if (g->format == KVQ_FMT_HQ2B_HAD) bytes += (size_t)lanes * g->num_q_heads * D * 2;   // rotated q (fp16)
+  return bytes;
 }
 
 size_t kvq_prefill_workspace_bytes(const kvq_geom* g, int n_q_rows, int max_seq_len) {
@@ -175,11 +184,11 @@ int kv_quant_append(const kvq_geom* g, int layer, void* pool, size_t pool_bytes,
   if (lanes == 0 || max_new == 0) return KVQ_OK;
   if (!pool || !page_table || !start_pos || !n_new || !tok_offset || !k || !v || !d_status)
     return KVQ_ERR_INVALID_ARG;
-  if (g->format == KVQ_FMT_HQ2B && !ring) return KVQ_ERR_INVALID_ARG;
+  if (two_bit(g->format) && !ring) return KVQ_ERR_INVALID_ARG;
   if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(pool) || !aligned16(ring) || !aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
   CacheView c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, 0, d_status);
-  return launch_append(g->format, c, static_cast<uint8_t*>(pool), static_cast<__nv_bfloat16*>(ring), start_pos,
+  return launch_append(layout_fmt(g->format), c, static_cast<uint8_t*>(pool), static_cast<__nv_bfloat16*>(ring), start_pos,
                        n_new, tok_offset, max_new, n_rows, lanes, static_cast<const __nv_bfloat16*>(k),
                        static_cast<const __nv_bfloat16*>(v), (cudaStream_t)stream);
 }
@@ -194,7 +203,13 @@ int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t poo
   if (ws_bytes < kvq_decode_workspace_bytes(g, lanes, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
   AttnArgs a = decode_args(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
                            max_seq_len, q, sm_scale, workspace, out, d_status);
-  if (g->format == KVQ_FMT_HQ2B) return launch_decode_hq2b(a, (cudaStream_t)stream);
+  if (g->format == KVQ_FMT_HQ2B_HAD) {
+    if (lanes > 8192) return KVQ_ERR_UNSUPPORTED;
+    // the rotated query sits after the partials
+    a.q_rot = reinterpret_cast<__half*>(static_cast<uint8_t*>(workspace) +
+                                        partial_bytes(lanes, g->num_q_heads, a.max_splits));
+  }
+  if (two_bit(g->format)) return launch_decode_hq2b(a, (cudaStream_t)stream);
   return launch_attn_generic(g->format, a, 1, (cudaStream_t)stream);
 }
 
@@ -206,6 +221,7 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
   int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
                              max_seq_len, q, workspace, out, d_status);
   if (rc) return rc;
+  if (g->format == KVQ_FMT_HQ2B_HAD) return KVQ_ERR_UNSUPPORTED;   // no rotated prefill kernel
   if (max_n_q < 0 || n_q_rows < 0) return KVQ_ERR_INVALID_ARG;
   if (lanes == 0 || max_n_q == 0) return KVQ_OK;
   if (!q_pos0 || !n_q || !q_offset) return KVQ_ERR_INVALID_ARG;
@@ -253,7 +269,7 @@ int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes,
   rc = kv_quant_append(g, layer, pool, pool_bytes, ring, page_table, max_pages, lanes, start_pos, n_new, tok_offset,
                        1, n_rows, k, v, d_status, stream);
   if (rc) return rc;
-  if (g->format != KVQ_FMT_HQ2B || lanes > 8192)   // BF16 pages or very many lanes: plain decode after it
+  if (g->format != KVQ_FMT_HQ2B || lanes > 8192)   // BF16 or rotated pages, very many lanes: plain decode
     return paged_decode_attn(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
                              max_seq_len, q, sm_scale, workspace, ws_bytes, out, d_status, stream);
   AttnArgs a = decode_args(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,

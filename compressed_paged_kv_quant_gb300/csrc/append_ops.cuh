@@ -49,14 +49,7 @@ __device__ __forceinline__ bool row8_ok(uint4 w) {
 // V row quantization by one warp, per token and 128-dim half (lanes 0-15: dims 0..127, lanes
 // 16-31: dims 128..255): lane l holds dims 8l..8l+7 of the row (bf16) in vx and gets their 2-bit
 // codes (16 bits, dim 8l+j at bits 2j) and the meta word of its half (s | z << 16, fp16 each).
-__device__ __forceinline__ void quant_v_row(uint4 vx, uint32_t& packed, uint32_t& meta) {
-  const uint32_t u[4] = {vx.x, vx.y, vx.z, vx.w};
-  float x[8];
-#pragma unroll
-  for (int j = 0; j < 4; j++) {
-    x[2 * j] = bf16_lo(u[j]);
-    x[2 * j + 1] = bf16_hi(u[j]);
-  }
+__device__ __forceinline__ void quant_v_row_f32(const float (&x)[8], uint32_t& packed, uint32_t& meta) {
   float mn = x[0], mx = x[0];
 #pragma unroll
   for (int j = 1; j < 8; j++) {
@@ -83,6 +76,35 @@ __device__ __forceinline__ void quant_v_row(uint4 vx, uint32_t& packed, uint32_t
     packed |= (uint32_t)code << (2 * j);
   }
   meta = (uint32_t)__half_as_ushort(sh) | ((uint32_t)__half_as_ushort(zh) << 16);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(uint4 w, float (&x)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; j++) {
+    x[2 * j] = bf16_lo(u[j]);
+    x[2 * j + 1] = bf16_hi(u[j]);
+  }
+}
+
+__device__ __forceinline__ void quant_v_row(uint4 vx, uint32_t& packed, uint32_t& meta) {
+  float x[8];
+  bf16x8_to_f32(vx, x);
+  quant_v_row_f32(x, packed, meta);
+}
+
+// The rotated format's V row: Walsh-Hadamard transform of the row (all 32 lanes), then the same
+// quantizer; false (on every lane) when a rotated value is not finite in fp16.
+__device__ __forceinline__ bool quant_v_row_rot(uint4 vx, uint32_t& packed, uint32_t& meta) {
+  float x[8];
+  bf16x8_to_f32(vx, x);
+  warp_fwht256(x);
+  bool ok = true;
+#pragma unroll
+  for (int j = 0; j < 8; j++) ok = ok && finite16(x[j]);
+  if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+  quant_v_row_f32(x, packed, meta);
+  return true;
 }
 
 // Page-close quantization of K, per channel over the page's 64 keys, by PARTS x 256 threads:
@@ -149,6 +171,64 @@ __device__ __forceinline__ bool kclose_core(const AppendArgs& a, int b, int h, i
   return true;
 }
 
+// kclose_core for the rotated format, by exactly 1,024 threads: warp w rotates keys w and w + 32
+// (lane l holds channels 8l .. 8l+7 of the rotated key), the channel maxima meet in shared
+// memory, and each lane writes the 2 code bytes of its channels for both keys.  The per-element
+// arithmetic is kclose_core's, on the rotated values.
+__device__ __forceinline__ bool kclose_core_rot(const AppendArgs& a, int b, int h, int p, int start, int off,
+                                                uint8_t* codes, __half* scales) {
+  const CacheView& c = a.c;
+  const int H = c.num_kv_heads;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  float x[2][8];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    const int t = w + 32 * i, pos = p * P + t;
+    const uint4 kw = pos < start ? reinterpret_cast<const uint4*>(a.ring + ring_row_offset(c, b, h, t))[lane]
+                                 : reinterpret_cast<const uint4*>(a.k + ((int64_t)(off + pos - start) * H + h) * D)[lane];
+    bf16x8_to_f32(kw, x[i]);
+#pragma unroll
+    for (int e = 0; e < 8; e++) bad |= !finite16(x[i][e]);
+    warp_fwht256(x[i]);
+#pragma unroll
+    for (int e = 0; e < 8; e++) bad |= !finite16(x[i][e]);
+  }
+  __shared__ float part_max[32][D];
+#pragma unroll
+  for (int e = 0; e < 8; e++) part_max[w][8 * lane + e] = fmaxf(fabsf(x[0][e]), fabsf(x[1][e]));
+  if (__syncthreads_or(bad)) return false;
+  if (threadIdx.x < D) {
+    const int d = threadIdx.x;
+    float m = part_max[0][d];
+    for (int i = 1; i < 32; i++) m = fmaxf(m, part_max[i][d]);
+    scales[d] = __float2half_rn(__fdiv_rn(m, 3.0f));
+  }
+  __syncthreads();
+  float sf[8];
+#pragma unroll
+  for (int e = 0; e < 8; e++) sf[e] = __half2float(scales[8 * lane + e]);
+#pragma unroll
+  for (int i = 0; i < 2; i++) {
+    uint32_t bits = 0;
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+      int code = 2;
+      if (sf[e] != 0.0f) {
+        float q = __fdiv_rn(x[i][e], sf[e]);
+        q = __fadd_rn(q, 3.0f);
+        q = __fmul_rn(0.5f, q);
+        q = fminf(fmaxf(rintf(q), 0.0f), 3.0f);
+        code = (int)q;
+      }
+      bits |= (uint32_t)code << (2 * e);
+    }
+    reinterpret_cast<uint16_t*>(codes + (w + 32 * i) * HQ2B_ROW)[lane] = (uint16_t)bits;
+  }
+  __syncthreads();
+  return true;
+}
+
 // Whether page p of lane b can take a K block: inside the table and mapped to a pool page
 // (flags and returns false otherwise; the same answer on every thread).
 __device__ __forceinline__ bool kblock_page_ok(const CacheView& c, int b, int p) {
@@ -183,7 +263,9 @@ __device__ __forceinline__ void kclose_page(const AppendArgs& a, int b, int h, i
   if (!kblock_page_ok(a.c, b, p)) return;
   __shared__ __align__(16) uint8_t codes[P * HQ2B_ROW];
   __shared__ __align__(16) __half scales[D];
-  if (!kclose_core<PARTS>(a, b, h, p, start, off, codes, scales)) {
+  const bool ok = (PARTS == 4 && a.c.rotated) ? kclose_core_rot(a, b, h, p, start, off, codes, scales)
+                                              : kclose_core<PARTS>(a, b, h, p, start, off, codes, scales);
+  if (!ok) {
     if (threadIdx.x == 0) flag(a.c.status, KVQ_STATUS_BAD_INPUT);
     return;
   }
@@ -224,7 +306,14 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, int b, int h, in
     return;
   }
   uint32_t packed, meta;
-  quant_v_row(vx, packed, meta);
+  if (c.rotated) {
+    if (!quant_v_row_rot(vx, packed, meta)) {
+      if (lane == 0) flag(c.status, KVQ_STATUS_BAD_INPUT);
+      return;
+    }
+  } else {
+    quant_v_row(vx, packed, meta);
+  }
   reinterpret_cast<uint16_t*>(vblk + slot * HQ2B_ROW)[lane] = (uint16_t)packed;
   if ((lane & 15) == 0) reinterpret_cast<uint32_t*>(vblk + HQ2B_META_OFF + slot * 8)[lane >> 4] = meta;
   if (i >= n - P) reinterpret_cast<uint4*>(a.ring + ring_row_offset(c, b, h, slot))[lane] = kx;

@@ -32,6 +32,7 @@ struct AttnArgs {
   int min_wp;        // fast 2-bit decode: least pages per warp (bounds the partials per lane/head)
   int max_seq_len;   // host bound on every seq_len[b]
   StepAppend step;   // fused decode step only (active == 0 otherwise)
+  __half* q_rot;     // rotated format: H q per (lane, query head) in fp16 (workspace), else null
 };
 
 // Resolve query i of lane b: its row, position, and key count.  Returns false (after

@@ -91,12 +91,19 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 }
 
 // A-operand pairs straight from a code word.  A 16-bit half holding code byte(s) with the code
-// of position i at bits 2k + 2i, 2k + 2i + 1 reads as the fp16 number M + c once every other bit
-// is masked off and the exponent of M = 2^(10 - 2k - 2i) is OR-ed in (one LOP3); M + c is exact.
-//   keys:   k = 1 (the word shifted left by 2, or right by 6 for its high byte): M = 256, 64, 16, 4;
-//           the MMA takes M + c as is and a per-page correction removes the M + 1.5 part.
-//   values: k = 0 (the word as is, or shifted right by 8): M = 1024, 256, 64, 16; one HSUB2
-//           (FMA pipe) turns M + c into c exactly.
+// of position i at bits e + 2i, e + 2i + 1 reads as the fp16 number M + c once every other bit
+// is masked off and the exponent of M = 2^(10 - e - 2i) is OR-ed in (one LOP3); M + c is exact.
+//   keys:   e = 2 (the word shifted left by 2, or right by 6 for its high byte): M = 256, 64, 16,
+//           4; the MMA takes M + c as is and a per-page correction removes the M + 1.5 part.
+//   values, plain: e = 0 (the word as is, or shifted right by 8): M = 1024, 256, 64, 16; one
+//           HSUB2 (FMA pipe) of M turns M + c into the code c exactly.
+//   values, centred: e = 1 (the word shifted left by 1, or right by 7): M = 512, 128, 32, 8; one
+//           HSUB2 of M + 1.5 (exact in fp16 only for M <= 512) gives c - 1.5 exactly, and the
+//           zero point becomes z + 1.5 s.  The rotated format needs this: the fp16 rounding of
+//           P (.) s_v scales the whole code row, whose mean is 1.5, and the inverse rotation
+//           gathers that common part onto output dims 0 and 128; the centred row has mean ~0.
+//           It costs one shift per code word and one FMA per meta entry (~2% of a decode call),
+//           so the plain format keeps the first form.
 __device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask, uint32_t magic) {
   return (x & mask) | magic;
 }
@@ -105,12 +112,23 @@ __device__ __forceinline__ uint32_t h2sub(uint32_t a, uint32_t b) {
   return *reinterpret_cast<uint32_t*>(&r);
 }
 constexpr uint32_t KMASK0 = 0x000C000Cu;   // key code position i: KMASK0 << 2i after the shift
-constexpr uint32_t VMASK0 = 0x00030003u;   // value code position i: VMASK0 << 2i
-// fp16x2 bit patterns: M + 0 for keys (256, 64, 16, 4) and values (1024, 256, 64, 16), and the
-// key correction M + 1.5 (257.5, 65.5, 17.5, 5.5), all exact in fp16
+// value code position i: VMASK << 2i after the shift (plain, centred)
+constexpr uint32_t VMASK_PLAIN = 0x00030003u, VMASK_CENTRED = 0x00060006u;
+// fp16x2 bit patterns: M + 0 for keys (256, 64, 16, 4) and values (plain 1024, 256, 64, 16;
+// centred 512, 128, 32, 8), the key correction M + 1.5 (257.5, 65.5, 17.5, 5.5) and the value
+// centring M + 1.5 (513.5, 129.5, 33.5, 9.5), all exact in fp16
 __constant__ uint32_t c_kmag[4] = {0x5C005C00u, 0x54005400u, 0x4C004C00u, 0x44004400u};
 __constant__ uint32_t c_kcor[4] = {0x5C065C06u, 0x54185418u, 0x4C604C60u, 0x45804580u};
 __constant__ uint32_t c_vmag[4] = {0x64006400u, 0x5C005C00u, 0x54005400u, 0x4C004C00u};
+__constant__ uint32_t c_vmag_cen[4] = {0x60006000u, 0x58005800u, 0x50005000u, 0x48004800u};
+__constant__ uint32_t c_vcen[4] = {0x60036003u, 0x580C580Cu, 0x50305030u, 0x48C048C0u};
+
+// 1.5 s + c in float for a fp16 s (one mixed-precision FMA; 1.5 s is exact, so one rounding)
+__device__ __forceinline__ float fma_h15_f(uint16_t s, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;\n" : "=f"(d) : "h"(s), "h"((uint16_t)0x3E00u), "f"(c));
+  return d;
+}
 
 // lazy rescale: the running max of a head moves only when a page max exceeds it by more than
 // RESCALE_LOG2 (log2 domain), so P <= 2^0.5 and P * s_v stays below 65,504 for any finite V
@@ -202,6 +220,7 @@ __device__ __forceinline__ bool page_phys(const CacheView& c, const Cursor& cu, 
 // Warp pairs: warp w < DEC_PAIRS runs Q.K^T + softmax of a page, warp w + DEC_PAIRS runs its
 // P.V one page behind; both walk the same range of pages.  Each warp streams its own half of
 // every page (K block / V block, 4,608 B each) through a 2-slot TMA ring.
+template <bool CENTRED>
 __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_main(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& c = a.c;
@@ -320,7 +339,10 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
     auto load_q = [&](int b, int h) {
       uint32_t w[32];
       if (r < G) {
-        const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + r) * D + 64 * cq);
+        // rotated format: H q (fp16, written by rotate_q_kernel), else q (bf16)
+        const int64_t qo = ((int64_t)b * Hq + h * G + r) * D + 64 * cq;
+        const uint4* src = a.c.rotated ? reinterpret_cast<const uint4*>(a.q_rot + qo)
+                                       : reinterpret_cast<const uint4*>(a.q + qo);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
           const uint4 v = src[i];
@@ -330,7 +352,10 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
 #pragma unroll
         for (int i = 0; i < 32; i++) w[i] = 0u;
       }
-      auto qf = [&](int e) { return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]); };
+      auto qf = [&](int e) {
+        if (a.c.rotated) return half_bits_to_float((uint16_t)((e & 1) ? w[e >> 1] >> 16 : w[e >> 1] & 0xFFFFu));
+        return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+      };
 #pragma unroll
       for (int jw = 0; jw < 4; jw++) {
         uint32_t p0[4], p1[4];
@@ -465,9 +490,12 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
 #pragma unroll
       for (int e = 0; e < 4; e++) O[i][e] = 0.f;
     const int t0 = perm_row(2 * cq), t1 = perm_row(2 * cq + 1);
-    uint32_t vmag[4];
+    uint32_t vmag[4], vcen[4];
 #pragma unroll
-    for (int i = 0; i < 4; i++) vmag[i] = c_vmag[i];
+    for (int i = 0; i < 4; i++) {
+      vmag[i] = CENTRED ? c_vmag_cen[i] : c_vmag[i];
+      vcen[i] = CENTRED ? c_vcen[i] : 0u;
+    }
     for (int j = 0; j < n_units; j++) {
       const int slot = j & 1;
       const uint32_t par = (j >> 1) & 1;
@@ -487,8 +515,9 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
       if (valid & (1u << slot)) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_VFULL + slot), par))) { timed_out = true; break; }
         const uint8_t* st = vring + slot * HQ2B_BLOCK;
-        // per m-tile: P (.) s_v per half (fp16), sum(P z), sum(P), the B fragments, then
-        // O^T += V^ . P'^T with a fp16 pair holding one dim of two tokens as the exact code c
+        // per m-tile: P (.) s_v per half (fp16), sum(P z') (z' = z, or z + 1.5 s_v centred),
+        // sum(P), the B fragments, then O^T += V^ . P'^T with a fp16 pair holding one dim of two
+        // tokens as the exact code c (or c - 1.5 centred)
 #pragma unroll
         for (int mt = 0; mt < 4; mt++) {
           const float4 pxm = xs[mt * 32 + lane];
@@ -498,8 +527,12 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
           for (int rr = 0; rr < 2; rr++) {
             const int tok = 16 * mt + 8 * rr + perm_row(r);
             const uint2 mw = *reinterpret_cast<const uint2*>(st + HQ2B_META_OFF + tok * 8);
-            const float z0 = half_bits_to_float((uint16_t)(mw.x >> 16));
-            const float z1 = half_bits_to_float((uint16_t)(mw.y >> 16));
+            float z0 = half_bits_to_float((uint16_t)(mw.x >> 16));
+            float z1 = half_bits_to_float((uint16_t)(mw.y >> 16));
+            if (CENTRED) {
+              z0 = fma_h15_f((uint16_t)(mw.x & 0xFFFFu), z0);
+              z1 = fma_h15_f((uint16_t)(mw.y & 0xFFFFu), z1);
+            }
             const float pa = pv[2 * rr], pb = pv[2 * rr + 1];
             l0 += pa;
             l1 += pb;
@@ -523,18 +556,21 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
             const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t1) * HQ2B_ROW);
             const uint32_t x[4] = {__byte_perm(w0, w1, 0x5410u), __byte_perm(w0, w1, 0x7632u),
                                    __byte_perm(w2, w3, 0x5410u), __byte_perm(w2, w3, 0x7632u)};
-            uint32_t hi[4];
+            uint32_t lo[4], hi[4];
 #pragma unroll
-            for (int k = 0; k < 4; k++) hi[k] = x[k] >> 8;
+            for (int k = 0; k < 4; k++) {
+              lo[k] = CENTRED ? x[k] << 1 : x[k];
+              hi[k] = x[k] >> (CENTRED ? 7 : 8);
+            }
 #pragma unroll
             for (int i8 = 0; i8 < 8; i8++) {
               const int pos = i8 & 3;
-              const uint32_t* src = i8 < 4 ? x : hi;
-              const uint32_t mk = VMASK0 << (2 * pos);
-              mma16816(O[8 * hf + i8], h2sub(lop_and_or(src[0], mk, vmag[pos]), vmag[pos]),
-                       h2sub(lop_and_or(src[1], mk, vmag[pos]), vmag[pos]),
-                       h2sub(lop_and_or(src[2], mk, vmag[pos]), vmag[pos]),
-                       h2sub(lop_and_or(src[3], mk, vmag[pos]), vmag[pos]), Bv[hf][0], Bv[hf][1]);
+              const uint32_t* src = i8 < 4 ? lo : hi;
+              const uint32_t mk = (CENTRED ? VMASK_CENTRED : VMASK_PLAIN) << (2 * pos);
+              mma16816(O[8 * hf + i8], h2sub(lop_and_or(src[0], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]),
+                       h2sub(lop_and_or(src[1], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]),
+                       h2sub(lop_and_or(src[2], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]),
+                       h2sub(lop_and_or(src[3], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]), Bv[hf][0], Bv[hf][1]);
             }
           }
         }
@@ -713,7 +749,7 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
     if ((lane & 15) == 0) s_vm[t_new][lane >> 4] = meta;
   }
   // ---- part 1b: tail scores; warp w takes keys w, w + 8, ..., four at a time, lanes over dims
-  float q[8];
+  float q[8], qc[8];   // q for keys from the ring; qc for keys from the codes (H q in the rotated format)
   {
     const uint4 w4 = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + j) * D)[lane];
     const uint32_t u[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -721,6 +757,18 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
     for (int i = 0; i < 4; i++) {
       q[2 * i] = bf16_lo(u[i]) * a.scale_log2;
       q[2 * i + 1] = bf16_hi(u[i]) * a.scale_log2;
+    }
+    if (c.rotated) {
+      const uint4 r4 = reinterpret_cast<const uint4*>(a.q_rot + ((int64_t)b * Hq + j) * D)[lane];
+      const uint32_t ru[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        qc[2 * i] = half_bits_to_float((uint16_t)(ru[i] & 0xFFFFu)) * a.scale_log2;
+        qc[2 * i + 1] = half_bits_to_float((uint16_t)(ru[i] >> 16)) * a.scale_log2;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; i++) qc[i] = q[i];
     }
   }
   // K channel scales of the closed page the tail starts in (dims 8 lane .. 8 lane + 7)
@@ -773,7 +821,7 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
       }
       float d = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; i++) d = fmaf(q[i], kx[i], d);
+      for (int i = 0; i < 8; i++) d = fmaf(pos >= ef ? q[i] : qc[i], kx[i], d);
       dot[u] = d;
     }
 #pragma unroll
@@ -893,7 +941,46 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
   __syncthreads();
   const float num = fmaf(acc, s_fin[0], s_red[0][d] + s_red[1][d] + s_red[2][d] + s_red[3][d]);
   const float den = s_fin[1];
-  a.out[((int64_t)b * Hq + j) * D + d] = den > 0.f ? num / den : 0.f;
+  const float o = den > 0.f ? num / den : 0.f;
+  if (!c.rotated) {
+    a.out[((int64_t)b * Hq + j) * D + d] = o;
+  } else {
+    // the pages hold H v: the merged output is H o, and H H = I turns it back
+    __syncthreads();
+    s_red[0][d] = o;
+    __syncthreads();
+    if (warp == 0) {
+      float x[8];
+#pragma unroll
+      for (int i = 0; i < 8; i++) x[i] = s_red[0][8 * lane + i];
+      warp_fwht256(x);
+      float4* dst = reinterpret_cast<float4*>(a.out + ((int64_t)b * Hq + j) * D + 8 * lane);
+      dst[0] = make_float4(x[0], x[1], x[2], x[3]);
+      dst[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+  }
+}
+
+// ----------------------------------------------------------------------------- rotated query
+// Rotated format: H q of every (lane, query head) in fp16, one warp per row.
+__global__ void __launch_bounds__(256) rotate_q_kernel(AttnArgs a) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= a.lanes * a.c.num_q_heads) return;
+  const uint4 w4 = reinterpret_cast<const uint4*>(a.q + (int64_t)row * D)[lane];
+  const uint32_t u[4] = {w4.x, w4.y, w4.z, w4.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    x[2 * i] = bf16_lo(u[i]);
+    x[2 * i + 1] = bf16_hi(u[i]);
+  }
+  warp_fwht256(x);
+  uint4 o;
+  o.x = pack_h2(x[0], x[1]);
+  o.y = pack_h2(x[2], x[3]);
+  o.z = pack_h2(x[4], x[5]);
+  o.w = pack_h2(x[6], x[7]);
+  reinterpret_cast<uint4*>(a.q_rot + (int64_t)row * D)[lane] = o;
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -942,9 +1029,16 @@ int launch_decode_hq2b(const AttnArgs& a_in, cudaStream_t stream) {
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
-    cudaFuncSetAttribute(decode_hq2b_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)(fixed + (2 * MAX_LANES_FAST + 1) * sizeof(int)));
+    const int max_smem = (int)(fixed + (2 * MAX_LANES_FAST + 1) * sizeof(int));
+    cudaFuncSetAttribute(decode_hq2b_main<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaFuncSetAttribute(decode_hq2b_main<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     attr_set[dev] = true;
+  }
+  // the rotated format takes the centred value codes (see the A-operand notes above)
+  void (*const main_kernel)(AttnArgs) = a.c.rotated ? decode_hq2b_main<true> : decode_hq2b_main<false>;
+  if (a.c.rotated) {
+    const int rows = a.lanes * a.c.num_q_heads;
+    rotate_q_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(a);
   }
   if (a.step.active) {
     // fused decode step: overlap the append kernel launched just before
@@ -958,9 +1052,9 @@ int launch_decode_hq2b(const AttnArgs& a_in, cudaStream_t stream) {
     mattr[0].val.programmaticStreamSerializationAllowed = 1;
     mc.attrs = mattr;
     mc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&mc, decode_hq2b_main, a) != cudaSuccess) return KVQ_ERR_CUDA;
+    if (cudaLaunchKernelEx(&mc, main_kernel, a) != cudaSuccess) return KVQ_ERR_CUDA;
   } else {
-    decode_hq2b_main<<<grid, DEC_PAIRS * 64, smem, stream>>>(a);
+    main_kernel<<<grid, DEC_PAIRS * 64, smem, stream>>>(a);
   }
   // the combine may start while the main grid drains; it waits for it before reading partials
   cudaLaunchConfig_t cfg = {};

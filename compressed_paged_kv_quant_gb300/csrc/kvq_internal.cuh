@@ -24,7 +24,7 @@ constexpr int GENERIC_SPLIT = 1024;   // decode, generic kernel
 constexpr int DECODE_SPLIT_HQ2B = 1024;
 constexpr int PREFILL_SPLIT = 8192;
 
-__host__ __device__ constexpr int block_bytes(int fmt) { return fmt == KVQ_FMT_HQ2B ? HQ2B_BLOCK : BF16_BLOCK; }
+__host__ __device__ constexpr int block_bytes(int fmt) { return fmt == KVQ_FMT_BF16 ? BF16_BLOCK : HQ2B_BLOCK; }
 
 // Everything a kernel needs to address one layer of the cache.
 struct CacheView {
@@ -38,6 +38,7 @@ struct CacheView {
   int layer;
   int window;
   int32_t* status;
+  int rotated;                // KVQ_FMT_HQ2B_HAD: page rows hold Walsh-Hadamard-rotated K and V
 };
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
@@ -66,6 +67,34 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
   return __half2float(__ushort_as_half(h));
+}
+
+// In-place 256-point Walsh-Hadamard transform of one row held by a warp (lane l holds elements
+// 8l .. 8l+7), normalized by 1/16 so that it is its own inverse.  Stages h = 1, 2, 4 inside a
+// lane, h = 8 .. 128 between lanes l and l ^ (h / 8); every butterfly is (a + b, a - b) with one
+// IEEE fp32 operation each, the lower index taking the sum.
+__device__ __forceinline__ void warp_fwht256(float (&x)[8]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = __fadd_rn(a, b);
+        x[i + h] = __fsub_rn(a, b);
+      }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = lane & m;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, x[i], m);
+      x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i++) x[i] = __fmul_rn(x[i], 0.0625f);
 }
 
 }  // namespace kvq

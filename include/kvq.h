@@ -42,7 +42,17 @@ extern "C" {
 
 typedef struct CUstream_st* kvq_stream_t; /* same handle as cudaStream_t; NULL = legacy stream */
 
-typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1 } kvq_format;
+/* KVQ_FMT_HQ2B_HAD: the HQ2B byte layout over K and V rows rotated by the normalized 256-point
+ * Walsh-Hadamard transform H (H = H^T = H^-1) before quantization -- the rotation that "Half the
+ * Cache, Twice the Context" ("What the vendors actually measured") credits with the accuracy
+ * change of a low-bit cache.  The quantizer's input is the fast transform in float (stages
+ * h = 1, 2, ..., 128, pairs (a + b, a - b), then x 1/16), so codes are reproducible bit for bit.
+ * The ring keeps keys as they came.  Decode rotates the query (q.k = Hq.Hk) and turns the output
+ * back (sum p Hv = H sum p v), so results approximate the same attention as HQ2B.
+ * kv_quant_append, paged_decode_attn (and _noalloc), kvq_decode_step and the page moves take it;
+ * paged_prefill_attn returns KVQ_ERR_UNSUPPORTED for it.  Its decode workspace is larger by
+ * lanes * num_q_heads * 512 B (the rotated query); kvq_decode_workspace_bytes counts it. */
+typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_HQ2B_HAD = 2 } kvq_format;
 
 typedef struct {
   int32_t format;       /* kvq_format */

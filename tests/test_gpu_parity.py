@@ -10,7 +10,7 @@ from oracle_side import assert_close, host_kv
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-HQ, BF = oracle.FMT_HQ2B, oracle.FMT_BF16
+HQ, BF, HAD = oracle.FMT_HQ2B, oracle.FMT_BF16, oracle.FMT_HQ2B_HAD
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -129,6 +129,29 @@ def test_append_bytes_independent_of_chunking(chunking):
     np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
 
 
+@pytest.mark.parametrize("chunking", ["one", "tokens", "random"])
+def test_rotated_append_bytes(chunking):
+    """The Walsh-Hadamard-rotated format: pool and ring bytes equal the oracle's, whatever the
+    call sizes (the rotated page close and V rows, the unrotated ring)."""
+    wl = _custom([300, 129, 64, 5], L=2, H=2, Hq=4)
+    dw = _dw(wl, HAD)
+    _gpu_fill(dw, chunking)
+    assert dw.cache.read_status() == 0
+    g, pool, ring = _oracle_full(wl, HAD)
+    np.testing.assert_array_equal(dw.cache.pool.cpu().numpy(), pool)
+    np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
+
+
+def test_rotated_format_refuses_prefill():
+    from compressed_paged_kv_quant_gb300 import kvq
+    wl = _custom([128], L=1, H=1, Hq=4)
+    dw = _dw(wl, HAD)
+    ws, out = dw.prefill_buffers(1)
+    with pytest.raises(kvq.KvqError) as e:
+        dw.prefill(0, dw.step_q(0), [127], [1], [0], ws, out)
+    assert e.value.code == kvq.ERR_UNSUPPORTED
+
+
 def test_bf16_append_bytes():
     wl = _custom([200, 64, 1], L=2, H=2, Hq=4)
     dw = _dw(wl, BF)
@@ -140,7 +163,7 @@ def test_bf16_append_bytes():
 LENS = [1, 63, 64, 65, 700, 1500, 2049, 3000]
 
 
-@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (HQ, 17), (BF, 0)])
+@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (HQ, 17), (BF, 0), (HAD, 0), (HAD, 64), (HAD, 17)])
 def test_decode_ragged_lanes(fmt, window):
     wl = _custom(LENS, L=2, H=2, Hq=12, window=window)
     dw = _dw(wl, fmt)
@@ -152,7 +175,7 @@ def test_decode_ragged_lanes(fmt, window):
         q = dw.step_q(layer)
         dw.decode(layer, q, ws, out)
         qh = np.concatenate([wl.q_np(layer, b, n - 1, 1) for b, n in enumerate(LENS)])
-        ref, st = oracle.decode(g, layer, pool, ring if fmt == HQ else None, window, wl.page_table, wl.lanes,
+        ref, st = oracle.decode(g, layer, pool, ring if fmt != BF else None, window, wl.page_table, wl.lanes,
                                 LENS, qh, dw.sm_scale)
         assert st == 0
         assert_close(out.cpu().numpy(), ref, what=f"decode fmt={fmt} W={window} layer={layer}")
