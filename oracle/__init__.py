@@ -23,6 +23,7 @@ _lib = None
 FMT_HQ2B = 0
 FMT_BF16 = 1
 FMT_HQ2B_HAD = 2   # the 2-bit format over Walsh-Hadamard-rotated K and V rows
+FMT_HQ2B_TOK = 3   # the 2-bit format with K quantized per token (V rule), no page close
 PAGE_OOB, LEN_GT_TABLE, BAD_INPUT, BAD_LEN = 1, 2, 4, 8
 
 

@@ -30,6 +30,12 @@
  *     normalized 256-point Walsh-Hadamard transform before quantization (rotation named as
  *     what makes low-bit caches work in "Half the Cache, Twice the Context"); the ring keeps
  *     keys unrotated, dequantized page rows are turned back with H (H = H^T = H^-1).
+ *   - per-token-K variant (format 3): the same 72 B rows, but each K row is quantized when it
+ *     is appended, per token and per 128-dim half, by the V rule (z, s, c; k^ = z + c*s) --
+ *     the axis that "Half the Cache, Twice the Context" ("What the cache loses when you round
+ *     it", reading 1) finds better for K at 2 bits on its 3-level grid.  There is no page
+ *     close; the ring still holds the last 64 keys exact, and a key is read from it only
+ *     inside the window (t >= seq_len - window).
  *   - accumulator model: "Half the Cache, Twice the Context", section "The cliff is in the
  *     accumulator, not the storage" (a running sum rounded after every add; two-level keeps
  *     an FP32 register).
@@ -47,6 +53,7 @@
 #define ORC_FMT_HQ2B 0
 #define ORC_FMT_BF16 1
 #define ORC_FMT_HQ2B_HAD 2   /* the 2-bit format over Walsh-Hadamard-rotated K and V rows */
+#define ORC_FMT_HQ2B_TOK 3   /* the 2-bit format with K quantized per token like V */
 
 /* status flags (same meaning as the device status word of the GPU library) */
 #define ORC_PAGE_OOB 1
@@ -121,7 +128,8 @@ double orc_kv_bytes_per_token(int layers, int kv_heads, int head_dim, double byt
 
 /* bytes one head's one token costs for K or for V in each format */
 int64_t orc_head_token_bytes(int format) {
-  if (format == ORC_FMT_HQ2B || format == ORC_FMT_HQ2B_HAD) return 64 + 8;   /* 64 B code + 8 B meta row */
+  if (format == ORC_FMT_HQ2B || format == ORC_FMT_HQ2B_HAD || format == ORC_FMT_HQ2B_TOK)
+    return 64 + 8;   /* 64 B code + 8 B meta row */
   if (format == ORC_FMT_BF16) return ORC_D * 2;
   return -1;
 }
@@ -272,7 +280,8 @@ void orc_dequant_k_row(const uint8_t* codes_row, const uint16_t* scales, double*
 
 /* ------------------------------------------------------------------ the paged cache */
 static int geom_ok(const orc_geom* g) {
-  return g && (g->format == ORC_FMT_HQ2B || g->format == ORC_FMT_BF16 || g->format == ORC_FMT_HQ2B_HAD) &&
+  return g && (g->format == ORC_FMT_HQ2B || g->format == ORC_FMT_BF16 || g->format == ORC_FMT_HQ2B_HAD ||
+               g->format == ORC_FMT_HQ2B_TOK) &&
          g->head_dim == ORC_D &&
          g->page_tokens == ORC_P && g->num_layers > 0 && g->num_kv_heads > 0 &&
          g->num_q_heads > 0 && g->num_q_heads % g->num_kv_heads == 0;
@@ -286,8 +295,10 @@ static uint16_t* ring_row(uint16_t* ring, const orc_geom* g, int lane, int layer
  * Append n_new[b] tokens to every lane b, one token at a time in position order.  Token row
  * tok_offset[b]+i of k/v ([rows][Hkv][256] bf16) lands at position start_pos[b]+i.  In the
  * 2-bit format the V row is quantized at once; the K row goes to ring slot pos % 64, and when
- * slot 63 is written the page closes and its K block is quantized from the ring.  In the BF16
- * format both rows are stored as they are.  Returns OR-ed status flags.
+ * slot 63 is written the page closes and its K block is quantized from the ring.  In the
+ * per-token-K format the K row is quantized at once as well (V rule, into the K block's code and
+ * meta rows) and also written to the ring; nothing happens at slot 63.  In the BF16 format both
+ * rows are stored as they are.  Returns OR-ed status flags.
  */
 int orc_append(const orc_geom* g, int layer, uint8_t* pool, int64_t pool_bytes, uint16_t* ring,
                const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
@@ -330,7 +341,11 @@ int orc_append(const orc_geom* g, int layer, uint8_t* pool, int64_t pool_bytes, 
         }
         memcpy(vblk + 4096 + slot * 8, meta, 8);
         memcpy(ring_row(ring, g, b, layer, h, slot), kx, ORC_D * 2);
-        if (slot == ORC_P - 1) {
+        if (g->format == ORC_FMT_HQ2B_TOK) {
+          /* the key row is quantized now, by the V rule, into the K block's own rows */
+          orc_quant_v_row(kx, kblk + slot * 64, meta);
+          memcpy(kblk + 4096 + slot * 8, meta, 8);
+        } else if (slot == ORC_P - 1) {
           uint16_t scales[ORC_D];
           if (g->format == ORC_FMT_HQ2B_HAD) {
             /* the page's 64 keys, each rotated, quantized per channel of the rotated basis */
@@ -361,13 +376,15 @@ int orc_append(const orc_geom* g, int layer, uint8_t* pool, int64_t pool_bytes, 
 }
 
 /* The key of position t as the attention sees it (double), given the lane's cache state of
- * seq_len tokens: in the 2-bit format keys at t >= min(seq_len - window, first position of
- * the open page) come from the exact ring, the rest are dequantized from their page. */
+ * seq_len tokens: in the 2-bit formats keys at t >= min(seq_len - window, first position of
+ * the open page) come from the exact ring (per-token-K format: t >= seq_len - window), the
+ * rest are dequantized from their page. */
 static int load_key(const orc_geom* g, int layer, const uint8_t* pool, int64_t npages,
                     const uint16_t* ring, int window, const int32_t* page_row, int max_pages,
                     int lane, int seq_len, int head, int64_t t, double* out) {
   int64_t open_start = (int64_t)(seq_len / ORC_P) * ORC_P;
   int64_t exact_from = seq_len - window < open_start ? seq_len - window : open_start;
+  if (g->format == ORC_FMT_HQ2B_TOK) exact_from = seq_len - window;   /* every key has codes */
   if (g->format != ORC_FMT_BF16 && t >= exact_from) {
     const uint16_t* r = ring_row((uint16_t*)ring, g, lane, layer, head, (int)(t % ORC_P));
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
@@ -381,6 +398,8 @@ static int load_key(const orc_geom* g, int layer, const uint8_t* pool, int64_t n
   if (g->format == ORC_FMT_BF16) {
     const uint16_t* r = (const uint16_t*)(blk + (int64_t)slot * ORC_D * 2);
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
+  } else if (g->format == ORC_FMT_HQ2B_TOK) {
+    orc_dequant_v_row(blk + slot * 64, (const uint16_t*)(blk + 4096 + slot * 8), out);
   } else {
     orc_dequant_k_row(blk + slot * 64, (const uint16_t*)(blk + 4096), out);
     if (g->format == ORC_FMT_HQ2B_HAD) {   /* the page holds H k: k^ = H (H k)^ */

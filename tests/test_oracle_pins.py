@@ -624,3 +624,128 @@ def test_rotated_format_attention_matches_unrotated_brute_force():
         w = np.exp(sc - sc.max())
         ref = (w @ vals) / w.sum()
         assert np.allclose(out[0, j], ref, atol=1e-10)
+
+
+# ----------------------------------------------------------------------------- per-token-K format
+def _grid_rows(rng, n, H):
+    """bf16 rows whose every 128-dim half sits on a 4-level grid z + {0,1,2,3}*s with fp16-exact
+    z and s, both ends present: the 2-bit V rule reproduces them exactly."""
+    zs = np.array([-1.5, -0.75, 0.25, -3.0, 2.0])
+    ss = np.array([1.0, 0.5, 0.25, 2.0, 0.125])
+    x = np.zeros((n, H, 256))
+    for t in range(n):
+        for h in range(H):
+            for half in range(2):
+                z, s = zs[rng.integers(5)], ss[rng.integers(5)]
+                c = rng.integers(0, 4, 128)
+                c[0], c[1] = 0, 3
+                rng.shuffle(c)
+                x[t, h, 128 * half:128 * (half + 1)] = z + c * s
+    assert np.array_equal(synth.bf16_bits_to_f32_np(_bf16(x)), x.astype(np.float32))
+    return _bf16(x), x
+
+
+@pytest.mark.parametrize("n,window", [(150, 0), (64, 0), (130, 17), (200, 64)])
+def test_tok_format_on_grid_rows_is_exact_attention(n, window):
+    """Per-token-K format, K and V rows already on the 2-bit grid: the quantization is lossless,
+    so the oracle's attention equals exact softmax attention over the inputs (numpy, double)
+    for every window, open page included."""
+    rng = np.random.default_rng(21 + n)
+    g = oracle.geom(oracle.FMT_HQ2B_TOK, 1, 2, 6)
+    pb = oracle.page_bytes(g)
+    npg = (n + 63) // 64
+    pool = _fill(npg + 2, pb)
+    ring = np.zeros((1, 1, 2, 64, 256), np.uint16)
+    pt = np.array([rng.permutation(npg + 2)[:npg]], np.int32)
+    k, kx = _grid_rows(rng, n, 2)
+    v, vx = _grid_rows(rng, n, 2)
+    assert oracle.append(g, 0, pool, ring, pt, 1, [0], [n], [0], k, v) == 0
+    q = _bf16(rng.standard_normal((1, 6, 256)))
+    out, st = oracle.decode(g, 0, pool, ring, window, pt, 1, [n], q, 0.0625)
+    assert st == 0
+    for j in range(6):
+        qj = synth.bf16_bits_to_f32_np(q[0, j]).astype(np.float64)
+        np.testing.assert_allclose(out[0, j], _softmax_attn(qj, kx[:, j // 3], vx[:, j // 3], 0.0625),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_tok_format_bytes_follow_the_v_rule():
+    """Per-token-K append: each K row's 64 code bytes and 8 meta bytes are the V rule applied to
+    that key (the V quantizer is pinned above); the V block equals the plain format's; no
+    page-close scales are written; the ring holds the last 64 keys."""
+    n = 130
+    g, pool, ring, pt, k, v = _tiny_cache(oracle.FMT_HQ2B_TOK, n, seed=3, pages=[2, 0, 4], pool_pages=5)
+    gp, poolp, ringp, _, _, _ = _tiny_cache(oracle.FMT_HQ2B, n, seed=3, pages=[2, 0, 4], pool_pages=5)
+    pb = oracle.page_bytes(g)
+    for t in range(n):
+        page = pool[pt[0, t // 64] * pb:][:pb]
+        pagep = poolp[pt[0, t // 64] * pb:][:pb]
+        s = t % 64
+        codes, meta = oracle.quant_v_row(k[t, 0])
+        assert np.array_equal(page[s * 64:(s + 1) * 64], codes)
+        assert np.array_equal(page[4096 + s * 8:4096 + s * 8 + 8].view(np.uint16), meta)
+        assert np.array_equal(page[4608:9216], pagep[4608:9216])
+    assert np.array_equal(ring, ringp)
+    # page 0 closed in the plain format (per-channel scales); the per-token format wrote meta rows
+    assert not np.array_equal(pool[2 * pb + 4096:2 * pb + 4608], poolp[2 * pb + 4096:2 * pb + 4608])
+
+
+def test_tok_format_reads_codes_of_the_open_page():
+    """Window 0: the per-token-K format reads every key from its codes (the open page too),
+    the plain format reads the open page from the ring; window 64 makes the last 64 keys exact
+    in both, so the two formats then differ only in how the closed pages' keys were coded."""
+    n = 100
+    gt, poolt, ringt, pt, k, v = _tiny_cache(oracle.FMT_HQ2B_TOK, n, seed=4)
+    q = _bf16(np.random.default_rng(15).standard_normal((1, 4, 256)))
+    out, st = oracle.decode(gt, 0, poolt, ringt, 0, pt, 1, [n], q, 0.0625)
+    assert st == 0
+    pb = oracle.page_bytes(gt)
+    K = np.zeros((n, 256))
+    V = np.zeros((n, 256))
+    for t in range(n):
+        page = poolt[pt[0, t // 64] * pb:][:pb]
+        s = t % 64
+        K[t] = oracle.dequant_v_row(page[s * 64:(s + 1) * 64], page[4096 + s * 8:][:8].view(np.uint16))
+        V[t] = oracle.dequant_v_row(page[4608 + s * 64:4608 + (s + 1) * 64], page[4608 + 4096 + s * 8:][:8].view(np.uint16))
+    kx = synth.bf16_bits_to_f32_np(k[:, 0]).astype(np.float64)
+    assert np.max(np.abs(K[64:] - kx[64:])) > 0.05                     # the open page is coded
+    for j in range(4):
+        qj = synth.bf16_bits_to_f32_np(q[0, j]).astype(np.float64)
+        np.testing.assert_allclose(out[0, j], _softmax_attn(qj, K, V, 0.0625), rtol=1e-12, atol=1e-12)
+    out64, _ = oracle.decode(gt, 0, poolt, ringt, 64, pt, 1, [n], q, 0.0625)
+    K[n - 64:] = kx[n - 64:]
+    for j in range(4):
+        qj = synth.bf16_bits_to_f32_np(q[0, j]).astype(np.float64)
+        np.testing.assert_allclose(out64[0, j], _softmax_attn(qj, K, V, 0.0625), rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- axis study
+def test_axis_study_reproduces_block2_tables():
+    """Half the Cache -- What the cache loses when you round it (Block 2 printed tables): the
+    study's page-grid part, same seed and draw order, prints the page's numbers."""
+    from oracle import axis_study
+    recon, needle = axis_study.page_tables()
+    want = golden("block2_axis_needle.txt")
+    want_r = [r[1:] for r in want if r[0] == "recon"]
+    want_n = [r[1:] for r in want if r[0] == "needle"]
+    assert [[c, str(b), f"{pt:.3e}", f"{pc:.3e}"] for c, b, pt, pc in recon] == want_r
+    assert [[str(kb), str(vb), f"{f}/200", f"{we:.2e}", f"{oe:.2e}"] for kb, vb, f, we, oe in needle] == want_n
+
+
+def test_axis_study_grids_are_the_oracle_quantizers():
+    """The study's 4-level rules are the format's: on bf16 inputs the V rule equals the oracle's
+    V row quantizer (both halves), and the K rule equals the oracle's page quantizer."""
+    from oracle import axis_study
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((64, 256))
+    x[:, ::16] *= 4
+    x[::7] *= 6
+    xb = _bf16(x)
+    xf = synth.bf16_bits_to_f32_np(xb).astype(np.float64)
+    for t in range(64):
+        want = oracle.dequant_v_row(*oracle.quant_v_row(xb[t]))
+        got = np.concatenate([axis_study.v_rule(xf[t:t + 1, :128], 1), axis_study.v_rule(xf[t:t + 1, 128:], 1)], 1)
+        np.testing.assert_array_equal(got[0], want)
+    codes, scales = oracle.quant_k_page(xb)
+    want = np.stack([oracle.dequant_k_row(codes[t], scales) for t in range(64)])
+    np.testing.assert_array_equal(axis_study.k_rule_per_channel(xf), want)
