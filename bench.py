@@ -30,7 +30,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 # page formats by name: the binding's (and the oracle's) format constant
-FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD"}
+FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD", "hq2b_tok": "FMT_HQ2B_TOK"}
 WORKLOAD = dict(lanes=8, ctx=40960, layers=16, kv_heads=4, q_heads=24)
 METRIC = "decode attn: compressed-KV tokens/s & achieved HBM GB/s (% of peak); prefill TFLOP/s"
 UNIT = "tokens/s"
@@ -377,12 +377,14 @@ def run_gpu(args):
                              "traffic": _decode_traffic() if args.format == "hq2b" else None,
                              "kernel": ("paged_decode_attn (decode_hq2b_main + decode_hq2b_combine), one layer"
                                         if args.format == "hq2b" else
-                                        "paged_decode_attn (rotate_q_kernel + decode_hq2b_main<centred> + "
-                                        "decode_hq2b_combine), one layer"),
+                                        ("paged_decode_attn (rotate_q_kernel + decode_hq2b_main<centred> + "
+                                         "decode_hq2b_combine), one layer") if args.format == "hq2b_had" else
+                                        "paged_decode_attn (decode_hq2b_main<per-token K> + decode_hq2b_combine), "
+                                        "one layer"),
                              "algorithmic_bytes_per_launch": attn_bytes},
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": (3 if args.format == "hq2b" else 4) * L * args.steps,
+                "gpu_launches": (4 if args.format == "hq2b_had" else 3) * L * args.steps,
                 "clocks": clk,
                 "prefill": prefill,
                 "page_moves": moves}
@@ -522,8 +524,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     ap.add_argument("--format", default="hq2b", choices=sorted(FORMATS),
-                    help="page format: hq2b (the benchmark's) or hq2b_had (Walsh-Hadamard-rotated 2-bit; "
-                         "decode only, no prefill)")
+                    help="page format: hq2b (the benchmark's), hq2b_had (Walsh-Hadamard-rotated 2-bit) or "
+                         "hq2b_tok (K per token); the variants time decode only")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-page-moves", action="store_true")
     ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],

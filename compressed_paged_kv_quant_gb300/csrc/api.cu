@@ -31,7 +31,8 @@ constexpr float LOG2E = 1.4426950408889634f;
 
 int check_geom(const kvq_geom* g) {
   if (!g) return KVQ_ERR_INVALID_ARG;
-  if (g->format != KVQ_FMT_HQ2B && g->format != KVQ_FMT_BF16 && g->format != KVQ_FMT_HQ2B_HAD)
+  if (g->format != KVQ_FMT_HQ2B && g->format != KVQ_FMT_BF16 && g->format != KVQ_FMT_HQ2B_HAD &&
+      g->format != KVQ_FMT_HQ2B_TOK)
     return KVQ_ERR_UNSUPPORTED;
   if (g->head_dim != D || g->page_tokens != P) return KVQ_ERR_UNSUPPORTED;
   if (g->num_layers <= 0 || g->num_kv_heads <= 0 || g->num_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
@@ -43,8 +44,8 @@ int check_geom(const kvq_geom* g) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// the byte layout a format uses: the rotated variant keeps HQ2B's
-int layout_fmt(int f) { return f == KVQ_FMT_HQ2B_HAD ? KVQ_FMT_HQ2B : f; }
+// the byte layout a format uses: the rotated and per-token-K variants keep HQ2B's
+int layout_fmt(int f) { return f == KVQ_FMT_HQ2B_HAD || f == KVQ_FMT_HQ2B_TOK ? KVQ_FMT_HQ2B : f; }
 bool two_bit(int f) { return layout_fmt(f) == KVQ_FMT_HQ2B; }
 
 size_t page_bytes_of(const kvq_geom* g) {
@@ -82,6 +83,7 @@ CacheView make_view(const kvq_geom* g, int layer, const void* pool, size_t pool_
   c.window = window;
   c.status = status;
   c.rotated = g->format == KVQ_FMT_HQ2B_HAD;
+  c.ktok = g->format == KVQ_FMT_HQ2B_TOK;
   return c;
 }
 
@@ -249,7 +251,9 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
     rc = launch_prefill_hq2b_tc(a, (cudaStream_t)stream);
     return rc ? rc : launch_attn_combine(a, 0, (cudaStream_t)stream);
   }
-  return launch_attn_generic(g->format, a, 0, (cudaStream_t)stream);
+  // BF16 pages, and the per-token-K format (its keys scale per token, which the tensor-core
+  // prefill's per-channel K tile does not): the CUDA-core split kernel
+  return launch_attn_generic(layout_fmt(g->format), a, 0, (cudaStream_t)stream);
 }
 
 int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes, void* ring, int window,

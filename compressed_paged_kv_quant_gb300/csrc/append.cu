@@ -14,6 +14,8 @@
 //      ring (only the chunk's last 64 tokens -- the ring keeps the newest key of each slot).
 // Launch 1 must read the ring before launch 2 overwrites it; stream order guarantees that.
 // Decode steps (max_new == 1): one launch does both for each (lane, head).
+// The per-token-K format (KVQ_FMT_HQ2B_TOK) codes the K row with the V rule in the rows pass and
+// has no page close.
 // All quantizer arithmetic is IEEE fp32 round-to-nearest-even (__fdiv_rn, __fsub_rn, ...,
 // never contracted into FMAs) so the bytes match a CPU implementation of the same steps.
 #include "append_ops.cuh"
@@ -57,7 +59,7 @@ __global__ void __launch_bounds__(KCLOSE_THREADS) append_one_kernel(AppendArgs a
   int start, n, off;
   if (!read_lane(a, b, start, n, off) || n == 0) return;
   if (threadIdx.x < 32) append_row<FMT>(a, b, h, 0, start, n, off);
-  if (FMT == KVQ_FMT_HQ2B && (start + 1) % P == 0) kclose_page(a, b, h, start / P, start, off);
+  if (FMT == KVQ_FMT_HQ2B && !a.c.ktok && (start + 1) % P == 0) kclose_page(a, b, h, start / P, start, off);
 }
 
 int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* ring, const int32_t* start_pos,
@@ -69,8 +71,10 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
     if (fmt == KVQ_FMT_HQ2B) append_one_kernel<KVQ_FMT_HQ2B><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
     else append_one_kernel<KVQ_FMT_BF16><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
   } else if (fmt == KVQ_FMT_HQ2B) {
-    dim3 gk(max_new / P + 1, c.num_kv_heads, lanes);
-    append_kclose_kernel<<<gk, KCLOSE_THREADS, 0, stream>>>(a);
+    if (!c.ktok) {   // the per-token-K format has no page close
+      dim3 gk(max_new / P + 1, c.num_kv_heads, lanes);
+      append_kclose_kernel<<<gk, KCLOSE_THREADS, 0, stream>>>(a);
+    }
     dim3 gr((max_new + ROWS_PER_CTA - 1) / ROWS_PER_CTA, lanes);
     append_rows_kernel<KVQ_FMT_HQ2B><<<gr, 256, 0, stream>>>(a);
   } else {

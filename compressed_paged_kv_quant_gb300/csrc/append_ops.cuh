@@ -272,8 +272,8 @@ __device__ __forceinline__ void kclose_page(const AppendArgs& a, int b, int h, i
   kblock_store(a, b, h, p, codes, scales);
 }
 
-// One warp: token i of lane b, head h -- V row quantization (HQ2B) or plain stores (BF16), and
-// the key into the ring (only the chunk's last 64 tokens: the ring keeps the newest key of each
+// One warp: token i of lane b, head h -- V row quantization (HQ2B; the K row too in the
+// per-token-K format) or plain stores (BF16), and the key into the ring (only the chunk's last 64 tokens: the ring keeps the newest key of each
 // slot).  Returns after flagging when the token is past the table or its page is invalid.
 template <int FMT>
 __device__ __forceinline__ void append_row(const AppendArgs& a, int b, int h, int i, int start, int n, int off) {
@@ -316,6 +316,11 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, int b, int h, in
   }
   reinterpret_cast<uint16_t*>(vblk + slot * HQ2B_ROW)[lane] = (uint16_t)packed;
   if ((lane & 15) == 0) reinterpret_cast<uint32_t*>(vblk + HQ2B_META_OFF + slot * 8)[lane >> 4] = meta;
+  if (c.ktok) {   // per-token-K format: the key row is coded now, by the V rule, in the K block
+    quant_v_row(kx, packed, meta);
+    reinterpret_cast<uint16_t*>(kblk + slot * HQ2B_ROW)[lane] = (uint16_t)packed;
+    if ((lane & 15) == 0) reinterpret_cast<uint32_t*>(kblk + HQ2B_META_OFF + slot * 8)[lane >> 4] = meta;
+  }
   if (i >= n - P) reinterpret_cast<uint4*>(a.ring + ring_row_offset(c, b, h, slot))[lane] = kx;
 }
 

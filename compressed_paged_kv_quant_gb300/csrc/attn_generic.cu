@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(128) attn_split_generic(AttnArgs a, int decode
 #pragma unroll
     for (int j = 0; j < 8; j++) acc[g][j] = 0.0f;
   }
-  const int ef = FMT == KVQ_FMT_HQ2B ? exact_from(len, c.window) : len;
+  const int ef = FMT == KVQ_FMT_HQ2B ? exact_from(len, c.window, c.ktok) : len;
   bool oob = false;
   for (int t = t0; t < t1; t++) {
     const uint8_t* page;
@@ -83,6 +83,14 @@ __global__ void __launch_bounds__(128) attn_split_generic(AttnArgs a, int decode
         kx[2 * j] = bf16_lo(u[j]);
         kx[2 * j + 1] = bf16_hi(u[j]);
       }
+    } else if (c.ktok) {
+      // per-token-K format: the key row is coded like a value row
+      const uint32_t codes = reinterpret_cast<const uint16_t*>(kblk + slot * HQ2B_ROW)[lane];
+      const uint32_t meta = reinterpret_cast<const uint32_t*>(kblk + HQ2B_META_OFF + slot * 8)[lane >> 4];
+      const float sk = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
+      const float zk = half_bits_to_float((uint16_t)(meta >> 16));
+#pragma unroll
+      for (int j = 0; j < 8; j++) kx[j] = zk + (float)((codes >> (2 * j)) & 3) * sk;
     } else {
       const uint32_t codes = reinterpret_cast<const uint16_t*>(kblk + slot * HQ2B_ROW)[lane];
       const uint4 sw = reinterpret_cast<const uint4*>(kblk + HQ2B_META_OFF)[lane];

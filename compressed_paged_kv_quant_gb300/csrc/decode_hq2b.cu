@@ -53,7 +53,7 @@ __device__ __forceinline__ int main_pages(const CacheView& c, const int32_t* seq
     if (bad) *bad = true;
     return 0;
   }
-  const int ef = exact_from(len, c.window);
+  const int ef = exact_from(len, c.window, c.ktok);
   return ef <= 0 ? 0 : ef / P;
 }
 
@@ -169,6 +169,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   return false;
 }
 
+// Dims of word jw (16 dims) of thread column cq in the Q.K^T contraction.  The plain layout
+// gives each thread 64 contiguous dims; the per-token-K layout keeps every k-step inside one
+// 128-dim half (jw 0-1: dims 0-127, jw 2-3: dims 128-255), since its keys scale per half.
+template <bool KTOK>
+__device__ __forceinline__ constexpr int dim_base(int cq, int jw) {
+  return KTOK ? 128 * (jw >> 1) + 32 * cq + 16 * (jw & 1) : 64 * cq + 16 * jw;
+}
+constexpr uint32_t H2_ONE = 0x3C003C00u;   // 1.0 in both fp16 lanes
+
 // QK row i of an m-tile holds token pi(i): swapping the two middle tokens of every group of
 // four makes the V-code loads of the P.V step hit shared-memory banks at most 2-way.
 __device__ __forceinline__ int perm_row(int i) { return i ^ ((i >> 1) & 1); }
@@ -220,7 +229,7 @@ __device__ __forceinline__ bool page_phys(const CacheView& c, const Cursor& cu, 
 // Warp pairs: warp w < DEC_PAIRS runs Q.K^T + softmax of a page, warp w + DEC_PAIRS runs its
 // P.V one page behind; both walk the same range of pages.  Each warp streams its own half of
 // every page (K block / V block, 4,608 B each) through a 2-slot TMA ring.
-template <bool CENTRED>
+template <bool CENTRED, bool KTOK>
 __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_main(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& c = a.c;
@@ -331,21 +340,22 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
 #pragma unroll
     for (int i = 0; i < 4; i++) {
       kmag[i] = c_kmag[i];
-      kcor[i] = c_kcor[i];
+      kcor[i] = KTOK ? 0u : c_kcor[i];
     }
-    // q of head r of the group, dims 64cq .. 64cq+63, as the fp16 B-fragment pairs of k-steps
-    // 4jw + i: (d, d+8) and (d+4, d+12) with d = 16jw + i; kept in shared memory, one uint4 =
-    // the 4 k-steps' first pairs or second pairs of one jw
+    float tk_mq[2][2], tk_q[2][2];   // per-token-K: sum_half q M and sum_half q, heads 2cq, 2cq+1
+    // q of head r of the group, the 64 dims dim_base(cq, jw) + 0..15 (jw = 0..3), as the fp16
+    // B-fragment pairs of k-steps 4jw + i: (d, d+8) and (d+4, d+12) with d = 16jw + i; kept in
+    // shared memory, one uint4 = the 4 k-steps' first pairs or second pairs of one jw
     auto load_q = [&](int b, int h) {
       uint32_t w[32];
       if (r < G) {
         // rotated format: H q (fp16, written by rotate_q_kernel), else q (bf16)
-        const int64_t qo = ((int64_t)b * Hq + h * G + r) * D + 64 * cq;
+        const int64_t qo = ((int64_t)b * Hq + h * G + r) * D;
         const uint4* src = a.c.rotated ? reinterpret_cast<const uint4*>(a.q_rot + qo)
                                        : reinterpret_cast<const uint4*>(a.q + qo);
 #pragma unroll
         for (int i = 0; i < 8; i++) {
-          const uint4 v = src[i];
+          const uint4 v = src[(dim_base<KTOK>(cq, i >> 1) + 8 * (i & 1)) / 8];
           w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
         }
       } else {
@@ -369,6 +379,29 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
         qsm[(2 * jw + 1) * 32 + lane] = make_uint4(p1[0], p1[1], p1[2], p1[3]);
       }
       __syncwarp();
+      if constexpr (KTOK) {
+        // per (lane, head) segment: sum over each half of q M and of q, per head of the thread's
+        // columns, from MMAs with constant A (every row the same)
+        float mq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        float qq[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int jw = 0; jw < 4; jw++) {
+          const uint4 qa = qsm[(2 * jw) * 32 + lane], qb = qsm[(2 * jw + 1) * 32 + lane];
+          const uint32_t q0[4] = {qa.x, qa.y, qa.z, qa.w}, q1[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+          for (int i = 0; i < 4; i++) {
+            mma16816(mq[jw >> 1], kmag[i], kmag[i], kmag[i], kmag[i], q0[i], q1[i]);
+            mma16816(qq[jw >> 1], H2_ONE, H2_ONE, H2_ONE, H2_ONE, q0[i], q1[i]);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; e++) {
+          tk_mq[0][e] = mq[0][e];
+          tk_mq[1][e] = mq[1][e];
+          tk_q[0][e] = qq[0][e];
+          tk_q[1][e] = qq[1][e];
+        }
+      }
     };
     load_q(cu.b, cu.h);
     for (int j = 0; j < n_units; j++) {
@@ -383,53 +416,86 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_KFULL + slot), par))) { timed_out = true; break; }
         const uint8_t* st = kring + slot * HQ2B_BLOCK;
         float Cc[4] = {0.f, 0.f, 0.f, 0.f};   // sum over dims of q~ (M + 1.5): the same for every key
+        float S1[4][4];                       // per-token-K: the second half's sums (S: the first)
 #pragma unroll
         for (int mt = 0; mt < 4; mt++)
 #pragma unroll
-          for (int e = 0; e < 4; e++) S[mt][e] = 0.f;
-        // k-step ks = 4j + i of thread column cq covers dims 64cq + 16j + {i, i+8} (A regs 0/1:
-        // codes of bytes 0/2 of word j) and {i+4, i+12} (A regs 2/3: bytes 1/3)
-        const uint8_t* krow_a = st + perm_row(r) * HQ2B_ROW + 16 * cq;
-        const uint8_t* krow_b = st + (8 + perm_row(r)) * HQ2B_ROW + 16 * cq;
-        const uint8_t* kscale = st + HQ2B_META_OFF + 128 * cq;
+          for (int e = 0; e < 4; e++) S[mt][e] = S1[mt][e] = 0.f;
+        // k-step ks = 4j + i of thread column cq covers dims dim_base(cq, j) + {i, i+8} (A regs
+        // 0/1: codes of bytes 0/2 of word j) and {i+4, i+12} (A regs 2/3: bytes 1/3)
+        const uint8_t* krow_a = st + perm_row(r) * HQ2B_ROW;
+        const uint8_t* krow_b = st + (8 + perm_row(r)) * HQ2B_ROW;
 #pragma unroll
         for (int jw = 0; jw < 4; jw++) {
-          const uint4 s_lo = *reinterpret_cast<const uint4*>(kscale + 32 * jw);
-          const uint4 s_hi = *reinterpret_cast<const uint4*>(kscale + 32 * jw + 16);
-          const uint32_t slo[4] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w};
-          const uint32_t shi[4] = {s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+          const int wbyte = dim_base<KTOK>(cq, jw) / 4;
           const uint4 qa = qsm[(2 * jw) * 32 + lane], qb = qsm[(2 * jw + 1) * 32 + lane];
           const uint32_t q0[4] = {qa.x, qa.y, qa.z, qa.w}, q1[4] = {qb.x, qb.y, qb.z, qb.w};
           uint32_t bq[4][2];
+          if constexpr (KTOK) {
+            // keys scaled per token: the B operand is q itself
 #pragma unroll
-          for (int i = 0; i < 4; i++) {
-            const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
-            bq[i][0] = h2mul(q0[i], __byte_perm(slo[i >> 1], shi[i >> 1], sel));
-            bq[i][1] = h2mul(q1[i], __byte_perm(slo[2 + (i >> 1)], shi[2 + (i >> 1)], sel));
-            mma16816(Cc, kcor[i], kcor[i], kcor[i], kcor[i], bq[i][0], bq[i][1]);
+            for (int i = 0; i < 4; i++) {
+              bq[i][0] = q0[i];
+              bq[i][1] = q1[i];
+            }
+          } else {
+            const uint8_t* kscale = st + HQ2B_META_OFF + 2 * dim_base<KTOK>(cq, jw);
+            const uint4 s_lo = *reinterpret_cast<const uint4*>(kscale);
+            const uint4 s_hi = *reinterpret_cast<const uint4*>(kscale + 16);
+            const uint32_t slo[4] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w};
+            const uint32_t shi[4] = {s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+              const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
+              bq[i][0] = h2mul(q0[i], __byte_perm(slo[i >> 1], shi[i >> 1], sel));
+              bq[i][1] = h2mul(q1[i], __byte_perm(slo[2 + (i >> 1)], shi[2 + (i >> 1)], sel));
+              mma16816(Cc, kcor[i], kcor[i], kcor[i], kcor[i], bq[i][0], bq[i][1]);
+            }
           }
 #pragma unroll
           for (int mt = 0; mt < 4; mt++) {
-            const uint32_t wa = *reinterpret_cast<const uint32_t*>(krow_a + 16 * mt * HQ2B_ROW + 4 * jw);
-            const uint32_t wb = *reinterpret_cast<const uint32_t*>(krow_b + 16 * mt * HQ2B_ROW + 4 * jw);
+            const uint32_t wa = *reinterpret_cast<const uint32_t*>(krow_a + 16 * mt * HQ2B_ROW + wbyte);
+            const uint32_t wb = *reinterpret_cast<const uint32_t*>(krow_b + 16 * mt * HQ2B_ROW + wbyte);
             const uint32_t la = wa << 2, ra = wa >> 6, lb = wb << 2, rb = wb >> 6;
+            float(&acc)[4] = (KTOK && jw >= 2) ? S1[mt] : S[mt];
 #pragma unroll
             for (int i = 0; i < 4; i++) {
               const uint32_t mk = KMASK0 << (2 * i);
-              mma16816(S[mt], lop_and_or(la, mk, kmag[i]), lop_and_or(lb, mk, kmag[i]), lop_and_or(ra, mk, kmag[i]),
+              mma16816(acc, lop_and_or(la, mk, kmag[i]), lop_and_or(lb, mk, kmag[i]), lop_and_or(ra, mk, kmag[i]),
                        lop_and_or(rb, mk, kmag[i]), bq[i][0], bq[i][1]);
             }
           }
         }
-        // q~ . k^ = 2 (sum q~ (M + c) - sum q~ (M + 1.5)), then the softmax scale (log2 domain)
-        const float k2 = 2.f * sl2;
-        const float cn0 = -Cc[0] * k2, cn1 = -Cc[1] * k2;
+        if constexpr (KTOK) {
+          // q . k^ = sum over halves of s (sum q (M + c) - sum q M) + z sum q, with the token's
+          // own (s, z) per half, then the softmax scale (log2 domain)
 #pragma unroll
-        for (int mt = 0; mt < 4; mt++) {
-          S[mt][0] = fmaf(S[mt][0], k2, cn0);
-          S[mt][1] = fmaf(S[mt][1], k2, cn1);
-          S[mt][2] = fmaf(S[mt][2], k2, cn0);
-          S[mt][3] = fmaf(S[mt][3], k2, cn1);
+          for (int mt = 0; mt < 4; mt++)
+#pragma unroll
+            for (int rr = 0; rr < 2; rr++) {
+              const uint2 mw = *reinterpret_cast<const uint2*>(st + HQ2B_META_OFF + (16 * mt + 8 * rr + perm_row(r)) * 8);
+              const float s0 = half_bits_to_float((uint16_t)(mw.x & 0xFFFFu)) * sl2;
+              const float z0 = half_bits_to_float((uint16_t)(mw.x >> 16)) * sl2;
+              const float s1 = half_bits_to_float((uint16_t)(mw.y & 0xFFFFu)) * sl2;
+              const float z1 = half_bits_to_float((uint16_t)(mw.y >> 16)) * sl2;
+#pragma unroll
+              for (int e = 0; e < 2; e++) {
+                const float c0 = fmaf(z0, tk_q[0][e], z1 * tk_q[1][e]);
+                S[mt][2 * rr + e] = fmaf(s0, S[mt][2 * rr + e] - tk_mq[0][e],
+                                         fmaf(s1, S1[mt][2 * rr + e] - tk_mq[1][e], c0));
+              }
+            }
+        } else {
+          // q~ . k^ = 2 (sum q~ (M + c) - sum q~ (M + 1.5)), then the softmax scale (log2 domain)
+          const float k2 = 2.f * sl2;
+          const float cn0 = -Cc[0] * k2, cn1 = -Cc[1] * k2;
+#pragma unroll
+          for (int mt = 0; mt < 4; mt++) {
+            S[mt][0] = fmaf(S[mt][0], k2, cn0);
+            S[mt][1] = fmaf(S[mt][1], k2, cn1);
+            S[mt][2] = fmaf(S[mt][2], k2, cn0);
+            S[mt][3] = fmaf(S[mt][3], k2, cn1);
+          }
         }
       }
       __syncwarp();
@@ -679,7 +745,7 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
   const int len = a.seq_len[b];
   const bool bad = len < 0 || len > c.max_pages * P;
   const int npg = bad ? 0 : main_pages(c, a.seq_len, b);
-  const int ef = bad ? 0 : exact_from(len, c.window);
+  const int ef = bad ? 0 : exact_from(len, c.window, c.ktok);
   const int tail_start = npg * P;
   const int ntail = bad ? 0 : len - tail_start;
   // fused decode step: this step's token (position len - 1) may still be being appended while
@@ -771,14 +837,15 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
       for (int i = 0; i < 8; i++) qc[i] = q[i];
     }
   }
-  // K channel scales of the closed page the tail starts in (dims 8 lane .. 8 lane + 7)
+  // K channel scales of the closed page the tail starts in (dims 8 lane .. 8 lane + 7); in the
+  // per-token-K format each code key brings its own (s, z) instead
   float ks[8];
   const uint8_t* kblk0 = nullptr;
   {
     uint4 sw = make_uint4(0u, 0u, 0u, 0u);
     if (tail_start < ef && s_phys[0] >= 0) {
       kblk0 = c.pool + (int64_t)s_phys[0] * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
-      sw = reinterpret_cast<const uint4*>(kblk0 + HQ2B_META_OFF)[lane];
+      if (!c.ktok) sw = reinterpret_cast<const uint4*>(kblk0 + HQ2B_META_OFF)[lane];
     }
     const __half2* sc = reinterpret_cast<const __half2*>(&sw);
 #pragma unroll
@@ -800,8 +867,10 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
           kw[u] = reinterpret_cast<const uint4*>(a.step.k + ((int64_t)st_off * H + h) * D)[lane];
         else if (pos >= ef)
           kw[u] = reinterpret_cast<const uint4*>(c.ring + ring_row_offset(c, b, h, pos % P))[lane];
-        else if (kblk0)
+        else if (kblk0) {
           kw[u].x = reinterpret_cast<const uint16_t*>(kblk0 + (pos % P) * HQ2B_ROW)[lane];
+          if (c.ktok) kw[u].y = reinterpret_cast<const uint32_t*>(kblk0 + HQ2B_META_OFF + (pos % P) * 8)[lane >> 4];
+        }
       }
     }
 #pragma unroll
@@ -815,6 +884,11 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
           kx[2 * i] = bf16_lo(w[i]);
           kx[2 * i + 1] = bf16_hi(w[i]);
         }
+      } else if (c.ktok) {
+        const float sk = half_bits_to_float((uint16_t)(kw[u].y & 0xFFFFu));
+        const float zk = half_bits_to_float((uint16_t)(kw[u].y >> 16));
+#pragma unroll
+        for (int i = 0; i < 8; i++) kx[i] = zk + (float)((kw[u].x >> (2 * i)) & 3u) * sk;
       } else {
 #pragma unroll
         for (int i = 0; i < 8; i++) kx[i] = ks[i] * (float)(2 * (int)((kw[u].x >> (2 * i)) & 3u) - 3);
@@ -1030,12 +1104,16 @@ int launch_decode_hq2b(const AttnArgs& a_in, cudaStream_t stream) {
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
     const int max_smem = (int)(fixed + (2 * MAX_LANES_FAST + 1) * sizeof(int));
-    cudaFuncSetAttribute(decode_hq2b_main<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-    cudaFuncSetAttribute(decode_hq2b_main<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaFuncSetAttribute(decode_hq2b_main<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaFuncSetAttribute(decode_hq2b_main<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    cudaFuncSetAttribute(decode_hq2b_main<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     attr_set[dev] = true;
   }
   // the rotated format takes the centred value codes (see the A-operand notes above)
-  void (*const main_kernel)(AttnArgs) = a.c.rotated ? decode_hq2b_main<true> : decode_hq2b_main<false>;
+  // and the per-token-K format its own Q.K^T step
+  void (*const main_kernel)(AttnArgs) = a.c.rotated ? decode_hq2b_main<true, false>
+                                        : a.c.ktok   ? decode_hq2b_main<false, true>
+                                                     : decode_hq2b_main<false, false>;
   if (a.c.rotated) {
     const int rows = a.lanes * a.c.num_q_heads;
     rotate_q_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(a);

@@ -39,6 +39,7 @@ struct CacheView {
   int window;
   int32_t* status;
   int rotated;                // KVQ_FMT_HQ2B_HAD: page rows hold Walsh-Hadamard-rotated K and V
+  int ktok;                   // KVQ_FMT_HQ2B_TOK: K rows coded per token like V (no page close)
 };
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
@@ -55,11 +56,11 @@ __device__ __forceinline__ int64_t ring_row_offset(const CacheView& c, int lane,
 }
 
 // First position whose key attention reads exact from the ring: min(len - W, start of the
-// page that is still open).
-__device__ __forceinline__ int exact_from(int len, int window) {
+// page that is still open); len - W in the per-token-K format, whose keys all have codes.
+__device__ __forceinline__ int exact_from(int len, int window, int ktok) {
   int open_start = (len / P) * P;
   int w = len - window;
-  return w < open_start ? w : open_start;
+  return ktok || w < open_start ? w : open_start;
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
   const int k1 = min(k0 + a.split_tokens, kmax);
   const int p0 = k0 / P;
   const int ntiles = (k1 + P - 1) / P - p0;
-  const int ef = exact_from(len, c.window);
+  const int ef = exact_from(len, c.window, c.ktok);
 
   uint8_t* smem = smem_raw + ((1024u - (sm_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 FMT_HQ2B = 0
 FMT_BF16 = 1
 FMT_HQ2B_HAD = 2   # the HQ2B layout over Walsh-Hadamard-rotated K and V rows
+FMT_HQ2B_TOK = 3   # the HQ2B layout with K rows coded per token (V rule), no page close
 
 OK = 0
 ERR_INVALID_ARG = -1

@@ -52,7 +52,15 @@ typedef struct CUstream_st* kvq_stream_t; /* same handle as cudaStream_t; NULL =
  * kv_quant_append, paged_decode_attn (and _noalloc), kvq_decode_step and the page moves take it;
  * paged_prefill_attn returns KVQ_ERR_UNSUPPORTED for it.  Its decode workspace is larger by
  * lanes * num_q_heads * 512 B (the rotated query); kvq_decode_workspace_bytes counts it. */
-typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_HQ2B_HAD = 2 } kvq_format;
+/* KVQ_FMT_HQ2B_TOK: the HQ2B byte layout with each K row coded when it is appended, per token
+ * and per 128-dim half, by the V rule (z = fp16(min), s = fp16((max - min)/3), k^ = z + c s):
+ * the K block holds 64 code rows + 64 meta rows like a V block, and there is no page close.
+ * This is the per-token axis that "Half the Cache, Twice the Context" ("What the cache loses
+ * when you round it") weighs against per-channel K.  The ring still keeps the last 64 keys
+ * exact; a key is read from it only inside the window (t >= seq_len - window), so with window 0
+ * every key, the open page's included, comes from its codes.  All calls take it; prefill runs
+ * on the CUDA-core split kernel. */
+typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_HQ2B_HAD = 2, KVQ_FMT_HQ2B_TOK = 3 } kvq_format;
 
 typedef struct {
   int32_t format;       /* kvq_format */

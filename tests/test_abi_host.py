@@ -47,6 +47,19 @@ def test_sizes_27b_geometry(L):
     assert kvq.decode_workspace_bytes(gh, 8, 40960) >= 8 * 24 * 40 * 258 * 4
 
 
+def test_two_bit_variants_share_the_layout(L):
+    """The rotated and per-token-K formats keep the 72 B rows of the 2-bit format and its ring;
+    the rotated one needs room for the rotated query in the decode workspace."""
+    gh = kvq.geom(kvq.FMT_HQ2B, 16, 4, 24)
+    for f in (kvq.FMT_HQ2B_HAD, kvq.FMT_HQ2B_TOK):
+        g = kvq.geom(f, 16, 4, 24)
+        assert kvq.page_bytes(g) == kvq.page_bytes(gh) == 64 * 9216
+        assert kvq.ring_bytes(g, 8) == kvq.ring_bytes(gh, 8)
+    base = kvq.decode_workspace_bytes(gh, 8, 40960)
+    assert kvq.decode_workspace_bytes(kvq.geom(kvq.FMT_HQ2B_TOK, 16, 4, 24), 8, 40960) == base
+    assert kvq.decode_workspace_bytes(kvq.geom(kvq.FMT_HQ2B_HAD, 16, 4, 24), 8, 40960) == base + 8 * 24 * 512
+
+
 @pytest.mark.parametrize("bad", [dict(head_dim=128), dict(page_tokens=32), dict(format=7),
                                  dict(num_q_heads=36), dict(num_q_heads=10)])
 def test_unsupported_geometry_is_refused(L, bad):

@@ -10,7 +10,7 @@ from oracle_side import assert_close, host_kv
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-HQ, BF, HAD = oracle.FMT_HQ2B, oracle.FMT_BF16, oracle.FMT_HQ2B_HAD
+HQ, BF, HAD, TOK = oracle.FMT_HQ2B, oracle.FMT_BF16, oracle.FMT_HQ2B_HAD, oracle.FMT_HQ2B_TOK
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -142,6 +142,19 @@ def test_rotated_append_bytes(chunking):
     np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
 
 
+@pytest.mark.parametrize("chunking", ["one", "tokens", "random"])
+def test_per_token_k_append_bytes(chunking):
+    """The per-token-K format: every K row coded at append by the V rule, no page close; pool
+    and ring bytes equal the oracle's whatever the call sizes."""
+    wl = _custom([300, 129, 64, 5], L=2, H=2, Hq=4)
+    dw = _dw(wl, TOK)
+    _gpu_fill(dw, chunking)
+    assert dw.cache.read_status() == 0
+    g, pool, ring = _oracle_full(wl, TOK)
+    np.testing.assert_array_equal(dw.cache.pool.cpu().numpy(), pool)
+    np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
+
+
 def test_rotated_format_refuses_prefill():
     from compressed_paged_kv_quant_gb300 import kvq
     wl = _custom([128], L=1, H=1, Hq=4)
@@ -163,7 +176,8 @@ def test_bf16_append_bytes():
 LENS = [1, 63, 64, 65, 700, 1500, 2049, 3000]
 
 
-@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (HQ, 17), (BF, 0), (HAD, 0), (HAD, 64), (HAD, 17)])
+@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (HQ, 17), (BF, 0), (HAD, 0), (HAD, 64), (HAD, 17),
+                                        (TOK, 0), (TOK, 64), (TOK, 17)])
 def test_decode_ragged_lanes(fmt, window):
     wl = _custom(LENS, L=2, H=2, Hq=12, window=window)
     dw = _dw(wl, fmt)
@@ -209,7 +223,7 @@ def test_decode_zero_length_lane_gives_zeros():
     assert torch.all(torch.isfinite(out))
 
 
-@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (BF, 0)])
+@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (BF, 0), (TOK, 0), (TOK, 64)])
 def test_prefill_chunks(fmt, window):
     """Causal chunks over a compressed prefix: (prefix, chunk) = (300, 100), (0, 70), (1000, 1100)."""
     prefix, chunk = [300, 0, 1000], [100, 70, 1100]
@@ -226,7 +240,7 @@ def test_prefill_chunks(fmt, window):
         q = torch.cat([wl.q_torch(layer, b, prefix[b], chunk[b], "cuda") for b in range(3)])
         dw.prefill(layer, q, prefix, chunk, offs, ws, out)
         qh = np.concatenate([wl.q_np(layer, b, prefix[b], chunk[b]) for b in range(3)])
-        ref, st = oracle.prefill(g, layer, pool, ring if fmt == HQ else None, window, wl.page_table, 3, prefix,
+        ref, st = oracle.prefill(g, layer, pool, ring if fmt != BF else None, window, wl.page_table, 3, prefix,
                                  chunk, offs, lens, qh, dw.sm_scale)
         assert st == 0
         assert_close(out.cpu().numpy(), ref, what=f"prefill fmt={fmt} W={window} layer={layer}")
