@@ -24,6 +24,7 @@ FMT_HQ2B = 0
 FMT_BF16 = 1
 FMT_HQ2B_HAD = 2   # the 2-bit format over Walsh-Hadamard-rotated K and V rows
 FMT_HQ2B_TOK = 3   # the 2-bit format with K quantized per token (V rule), no page close
+FMT_FP8 = 4        # K and V rows as FP8 E4M3 (one byte a value) with a per-tensor scale each
 PAGE_OOB, LEN_GT_TABLE, BAD_INPUT, BAD_LEN = 1, 2, 4, 8
 
 
@@ -40,11 +41,13 @@ def build(force: bool = False) -> str:
 class Geom(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("num_layers", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
 
-def geom(fmt: int, layers: int, kv_heads: int, q_heads: int) -> Geom:
-    return Geom(fmt, layers, kv_heads, q_heads, 256, 64)
+def geom(fmt: int, layers: int, kv_heads: int, q_heads: int, k_scale: float = 0.0, v_scale: float = 0.0) -> Geom:
+    """k_scale / v_scale: the FP8 format's per-tensor scales (0 means 1); other formats ignore them."""
+    return Geom(fmt, layers, kv_heads, q_heads, 256, 64, k_scale, v_scale)
 
 
 def lib():
@@ -85,6 +88,10 @@ def lib():
             L.orc_decode.restype = i32
             L.orc_prefill.argtypes = [G, i32, P, i64, P, i32, P, i32, i32, P, P, P, P, P, dbl, P]
             L.orc_prefill.restype = i32
+            L.orc_f32_to_e4m3.argtypes = [ctypes.c_float]
+            L.orc_f32_to_e4m3.restype = ctypes.c_uint8
+            L.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_to_f64.restype = dbl
             L.orc_flat_sum.argtypes = [i32, i32, i32]
             L.orc_flat_sum.restype = dbl
             _lib = L
@@ -114,6 +121,15 @@ def f32_to_f16(x: float) -> int:
 
 def f16_to_f32(h: int) -> float:
     return float(lib().orc_f16_to_f32(int(h)))
+
+
+def f32_to_e4m3(x: float) -> int:
+    """FP8 E4M3 byte of a float: round to nearest even, saturating at +-448."""
+    return int(lib().orc_f32_to_e4m3(x))
+
+
+def e4m3_to_f64(b: int) -> float:
+    return float(lib().orc_e4m3_to_f64(b))
 
 
 def round_bf16(x: float) -> float:

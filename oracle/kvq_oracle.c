@@ -36,6 +36,13 @@
  *     it", reading 1) finds better for K at 2 bits on its 3-level grid.  There is no page
  *     close; the ring still holds the last 64 keys exact, and a key is read from it only
  *     inside the window (t >= seq_len - window).
+ *   - FP8 format (format 4): K and V rows stored as OCP FP8 E4M3 values (1 sign, 4 exponent
+ *     bits with bias 7, 3 mantissa bits; no infinities; largest finite 448), one byte per value,
+ *     256 B per head per token each -- half the bytes of BF16, the "2x capacity" FP8 cache of the
+ *     vLLM study quoted in "Half the Cache, Twice the Context" ("What the vendors actually
+ *     measured").  A per-tensor scale per K and V (geometry fields; 0 means 1) divides the
+ *     input in fp32 before the conversion (round to nearest even, saturating at +-448) and
+ *     multiplies the decoded value.  No ring: every key and value is read from its page.
  *   - accumulator model: "Half the Cache, Twice the Context", section "The cliff is in the
  *     accumulator, not the storage" (a running sum rounded after every add; two-level keeps
  *     an FP32 register).
@@ -54,6 +61,7 @@
 #define ORC_FMT_BF16 1
 #define ORC_FMT_HQ2B_HAD 2   /* the 2-bit format over Walsh-Hadamard-rotated K and V rows */
 #define ORC_FMT_HQ2B_TOK 3   /* the 2-bit format with K quantized per token like V */
+#define ORC_FMT_FP8 4        /* K and V rows as FP8 E4M3 with a per-tensor scale each */
 
 /* status flags (same meaning as the device status word of the GPU library) */
 #define ORC_PAGE_OOB 1
@@ -63,6 +71,7 @@
 
 typedef struct {
   int32_t format, num_layers, num_kv_heads, num_q_heads, head_dim, page_tokens;
+  float k_scale, v_scale;   /* FP8 format only: per-tensor scales (0 means 1) */
 } orc_geom;
 
 /* ------------------------------------------------------------------ scalar conversions */
@@ -131,6 +140,7 @@ int64_t orc_head_token_bytes(int format) {
   if (format == ORC_FMT_HQ2B || format == ORC_FMT_HQ2B_HAD || format == ORC_FMT_HQ2B_TOK)
     return 64 + 8;   /* 64 B code + 8 B meta row */
   if (format == ORC_FMT_BF16) return ORC_D * 2;
+  if (format == ORC_FMT_FP8) return ORC_D;
   return -1;
 }
 
@@ -255,6 +265,47 @@ void orc_hadamard_f64(const double* x, double* y) {
   }
 }
 
+/* ------------------------------------------------------------------ FP8 E4M3
+ * Encode a float as E4M3 by the format's definition: the representable magnitudes below 2^-6
+ * are the multiples of 2^-9 (exponent field 0); from 2^e (e >= -6) up to 2^(e+1) they are the
+ * multiples of 2^(e-3).  Round to the nearest multiple, ties to even; magnitudes past 448 give
+ * 448 (saturation: the format has no infinity, and 464, the tie, also rounds to 448). */
+uint8_t orc_f32_to_e4m3(float x) {
+  uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  double a = fabs((double)x);
+  if (isnan(x)) return 0x7F;
+  if (a >= 448.0) return sign | 0x7E;
+  int ex;
+  frexp(a, &ex);                          /* a = f 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1 */
+  int e = a == 0.0 ? -6 : ex - 1;
+  if (e < -6) e = -6;
+  double quantum = ldexp(1.0, e - 3);
+  double n = a / quantum;                 /* exact: a power-of-two scaling */
+  double r = floor(n);
+  double frac = n - r;
+  if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  double v = r * quantum;                 /* the rounded magnitude, at most 448 */
+  if (v == 0.0) return sign;
+  if (v < ldexp(1.0, -6)) return sign | (uint8_t)(v / ldexp(1.0, -9));             /* subnormal */
+  frexp(v, &ex);
+  int E = ex - 1 + 7;
+  int m = (int)(v / ldexp(1.0, ex - 1) * 8.0) - 8;
+  return sign | (uint8_t)(E << 3) | (uint8_t)m;
+}
+
+double orc_e4m3_to_f64(uint8_t b) {
+  int E = (b >> 3) & 15, m = b & 7;
+  double s = (b & 0x80) ? -1.0 : 1.0;
+  if (E == 15 && m == 7) return NAN;
+  if (E == 0) return s * m * ldexp(1.0, -9);
+  return s * (1.0 + m / 8.0) * ldexp(1.0, E - 7);
+}
+
+static float fp8_scale(const orc_geom* g, int kv) {
+  float s = kv ? g->v_scale : g->k_scale;
+  return s == 0.0f ? 1.0f : s;
+}
+
 static int f32_ok(const float* x, int n) {
   for (int i = 0; i < n; i++)
     if (!(fabsf(x[i]) <= 65504.0f)) return 0;
@@ -280,8 +331,11 @@ void orc_dequant_k_row(const uint8_t* codes_row, const uint16_t* scales, double*
 
 /* ------------------------------------------------------------------ the paged cache */
 static int geom_ok(const orc_geom* g) {
+  if (g && g->format == ORC_FMT_FP8 &&
+      (!(g->k_scale >= 0.0f && g->k_scale <= 3.0e38f) || !(g->v_scale >= 0.0f && g->v_scale <= 3.0e38f)))
+    return 0;
   return g && (g->format == ORC_FMT_HQ2B || g->format == ORC_FMT_BF16 || g->format == ORC_FMT_HQ2B_HAD ||
-               g->format == ORC_FMT_HQ2B_TOK) &&
+               g->format == ORC_FMT_HQ2B_TOK || g->format == ORC_FMT_FP8) &&
          g->head_dim == ORC_D &&
          g->page_tokens == ORC_P && g->num_layers > 0 && g->num_kv_heads > 0 &&
          g->num_q_heads > 0 && g->num_q_heads % g->num_kv_heads == 0;
@@ -326,6 +380,14 @@ int orc_append(const orc_geom* g, int layer, uint8_t* pool, int64_t pool_bytes, 
         if (g->format == ORC_FMT_BF16) {
           memcpy(kblk + (int64_t)slot * ORC_D * 2, kx, ORC_D * 2);
           memcpy(vblk + (int64_t)slot * ORC_D * 2, vx, ORC_D * 2);
+          continue;
+        }
+        if (g->format == ORC_FMT_FP8) {   /* x / scale in fp32, then E4M3 */
+          float ks = fp8_scale(g, 0), vs = fp8_scale(g, 1);
+          for (int d = 0; d < ORC_D; d++) {
+            kblk[(int64_t)slot * ORC_D + d] = orc_f32_to_e4m3(orc_bf16_to_f32(kx[d]) / ks);
+            vblk[(int64_t)slot * ORC_D + d] = orc_f32_to_e4m3(orc_bf16_to_f32(vx[d]) / vs);
+          }
           continue;
         }
         uint16_t meta[4];
@@ -385,7 +447,7 @@ static int load_key(const orc_geom* g, int layer, const uint8_t* pool, int64_t n
   int64_t open_start = (int64_t)(seq_len / ORC_P) * ORC_P;
   int64_t exact_from = seq_len - window < open_start ? seq_len - window : open_start;
   if (g->format == ORC_FMT_HQ2B_TOK) exact_from = seq_len - window;   /* every key has codes */
-  if (g->format != ORC_FMT_BF16 && t >= exact_from) {
+  if (g->format != ORC_FMT_BF16 && g->format != ORC_FMT_FP8 && t >= exact_from) {
     const uint16_t* r = ring_row((uint16_t*)ring, g, lane, layer, head, (int)(t % ORC_P));
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
     return 0;
@@ -398,6 +460,8 @@ static int load_key(const orc_geom* g, int layer, const uint8_t* pool, int64_t n
   if (g->format == ORC_FMT_BF16) {
     const uint16_t* r = (const uint16_t*)(blk + (int64_t)slot * ORC_D * 2);
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
+  } else if (g->format == ORC_FMT_FP8) {
+    for (int d = 0; d < ORC_D; d++) out[d] = orc_e4m3_to_f64(blk[(int64_t)slot * ORC_D + d]) * fp8_scale(g, 0);
   } else if (g->format == ORC_FMT_HQ2B_TOK) {
     orc_dequant_v_row(blk + slot * 64, (const uint16_t*)(blk + 4096 + slot * 8), out);
   } else {
@@ -421,6 +485,8 @@ static int load_value(const orc_geom* g, int layer, const uint8_t* pool, int64_t
   if (g->format == ORC_FMT_BF16) {
     const uint16_t* r = (const uint16_t*)(blk + (int64_t)slot * ORC_D * 2);
     for (int d = 0; d < ORC_D; d++) out[d] = orc_bf16_to_f32(r[d]);
+  } else if (g->format == ORC_FMT_FP8) {
+    for (int d = 0; d < ORC_D; d++) out[d] = orc_e4m3_to_f64(blk[(int64_t)slot * ORC_D + d]) * fp8_scale(g, 1);
   } else {
     orc_dequant_v_row(blk + slot * 64, (const uint16_t*)(blk + 4096 + slot * 8), out);
     if (g->format == ORC_FMT_HQ2B_HAD) {   /* the page holds H v: v^ = H (H v)^ */

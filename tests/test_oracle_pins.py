@@ -749,3 +749,84 @@ def test_axis_study_grids_are_the_oracle_quantizers():
     codes, scales = oracle.quant_k_page(xb)
     want = np.stack([oracle.dequant_k_row(codes[t], scales) for t in range(64)])
     np.testing.assert_array_equal(axis_study.k_rule_per_channel(xf), want)
+
+
+# ----------------------------------------------------------------------------- FP8 format
+def test_e4m3_encoder_matches_torch_on_every_bf16():
+    """The oracle's E4M3 encoder (written from the format definition) against torch's
+    float8_e4m3fn conversion on every finite bf16 value below the rounding limit 464; past it
+    the encoder saturates to +-448 (torch gives NaN there: the format has no infinity)."""
+    u = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = synth.bf16_bits_to_f32_np(u)
+    fin = np.isfinite(x)
+    mine = np.array([oracle.f32_to_e4m3(float(v)) for v in x[fin]], np.uint8)
+    ref = torch.from_numpy(x[fin]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    small = np.abs(x[fin]) < 464
+    np.testing.assert_array_equal(mine[small], ref[small])
+    big = ~small
+    np.testing.assert_array_equal(mine[big], np.where(x[fin][big] < 0, 0xFE, 0x7E).astype(np.uint8))
+
+
+def test_e4m3_decoder_matches_torch_on_every_byte():
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    mine = np.array([oracle.e4m3_to_f64(int(v)) for v in b])
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(mine[ok], ref[ok])
+    assert oracle.e4m3_to_f64(0x7E) == 448.0 and oracle.e4m3_to_f64(0x01) == 2.0 ** -9
+
+
+@pytest.mark.parametrize("k_scale,v_scale", [(0.0, 0.0), (0.25, 3.0)])
+def test_fp8_format_bytes_and_attention_follow_torch(k_scale, v_scale):
+    """FP8 pages: every stored byte is torch's E4M3 of x / scale (fp32 division; in range here),
+    and the oracle's attention equals brute force over torch's decoded values times the scale."""
+    n, H, Hq = 150, 2, 6
+    g = oracle.geom(oracle.FMT_FP8, 1, H, Hq, k_scale, v_scale)
+    assert oracle.head_token_bytes(oracle.FMT_FP8) == 256
+    pb = oracle.page_bytes(g)
+    rng = np.random.default_rng(41)
+    npg = (n + 63) // 64
+    pt = np.array([rng.permutation(npg + 2)[:npg]], np.int32)
+    pool = _fill(npg + 2, pb)
+    xk = rng.standard_normal((n, H, 256))
+    xk[:, :, ::16] *= 4
+    xv = rng.standard_normal((n, H, 256))
+    xv[::64] *= 6
+    k, v = _bf16(xk), _bf16(xv)
+    assert oracle.append(g, 0, pool, None, pt, 1, [0], [n], [0], k, v) == 0
+    ks, vs = (k_scale or 1.0), (v_scale or 1.0)
+    kq = torch.from_numpy(synth.bf16_bits_to_f32_np(k) / np.float32(ks)).to(torch.float8_e4m3fn)
+    vq = torch.from_numpy(synth.bf16_bits_to_f32_np(v) / np.float32(vs)).to(torch.float8_e4m3fn)
+    for t in range(n):
+        page = pool[pt[0, t // 64] * pb:][:pb]
+        s = t % 64
+        for h in range(H):
+            kb = page[(h * 2) * 16384 + s * 256:][:256]
+            vb = page[(h * 2 + 1) * 16384 + s * 256:][:256]
+            np.testing.assert_array_equal(kb, kq[t, h].view(torch.uint8).numpy())
+            np.testing.assert_array_equal(vb, vq[t, h].view(torch.uint8).numpy())
+    K = kq.to(torch.float64).numpy() * ks
+    V = vq.to(torch.float64).numpy() * vs
+    q = _bf16(rng.standard_normal((1, Hq, 256)))
+    out, st = oracle.decode(g, 0, pool, None, 0, pt, 1, [n], q, 0.0625)
+    assert st == 0
+    for j in range(Hq):
+        qj = synth.bf16_bits_to_f32_np(q[0, j]).astype(np.float64)
+        np.testing.assert_allclose(out[0, j], _softmax_attn(qj, K[:, j // 3], V[:, j // 3], 0.0625),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_format_saturates_and_flags_bad_input():
+    g = oracle.geom(oracle.FMT_FP8, 1, 1, 4)
+    pb = oracle.page_bytes(g)
+    pool = np.zeros(pb, np.uint8)
+    pt = np.array([[0]], np.int32)
+    x = np.zeros((2, 1, 256), np.float32)
+    x[0, 0, 0], x[0, 0, 1], x[0, 0, 2] = 1000.0, -600.0, 450.0
+    k = _bf16(x)
+    assert oracle.append(g, 0, pool, None, pt, 1, [0], [1], [0], k, k) == 0
+    assert list(pool[:3]) == [0x7E, 0xFE, 0x7E]
+    k2 = k.copy()
+    k2[1, 0, 5] = 0x7F80                                 # +inf in bf16
+    assert oracle.append(g, 0, pool, None, pt, 1, [1], [1], [1], k2, k2) == oracle.BAD_INPUT
