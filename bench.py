@@ -30,7 +30,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 # page formats by name: the binding's (and the oracle's) format constant
-FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD", "hq2b_tok": "FMT_HQ2B_TOK"}
+FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD", "hq2b_tok": "FMT_HQ2B_TOK", "fp8": "FMT_FP8"}
+# bytes one head's one token costs for K plus V in each format
+KV_BYTES = {"hq2b": 144, "hq2b_had": 144, "hq2b_tok": 144, "fp8": 512}
 WORKLOAD = dict(lanes=8, ctx=40960, layers=16, kv_heads=4, q_heads=24)
 METRIC = "decode attn: compressed-KV tokens/s & achieved HBM GB/s (% of peak); prefill TFLOP/s"
 UNIT = "tokens/s"
@@ -73,12 +75,13 @@ def _decode_traffic():
     return None
 
 
-def _config(extra=None):
+def _config(extra=None, fmt="hq2b"):
+    pages = "FP8 E4M3 pages (256 B/head/token each for K and V)" if fmt == "fp8" else "2-bit pages (72 B/head/token)"
     c = {"workload": "decode_27b_8x40960: 16 layers x 4 KV heads x 256, 24 q heads, 8 lanes x 40,960 tokens, "
-                     "2-bit pages (72 B/head/token), append + decode per layer",
+                     f"{pages}, append + decode per layer",
          "lanes": WORKLOAD["lanes"], "context_tokens": WORKLOAD["ctx"], "layers": WORKLOAD["layers"],
          "kv_heads": WORKLOAD["kv_heads"], "q_heads": WORKLOAD["q_heads"], "head_dim": 256, "page_tokens": 64,
-         "pool_bytes": WORKLOAD["lanes"] * WORKLOAD["ctx"] * 9216,
+         "pool_bytes": WORKLOAD["lanes"] * WORKLOAD["ctx"] * WORKLOAD["layers"] * WORKLOAD["kv_heads"] * KV_BYTES[fmt],
          "l2_policy": "inputs larger than L2 (3.02 GB pool read per step)",
          "parallelism": "replicas only (one GPU per process)"}
     if extra:
@@ -323,7 +326,7 @@ def run_gpu(args):
         d1.record(stream)
     stream.synchronize()
     call_ms = d0.elapsed_time(d1) / (reps * L)
-    attn_bytes = lanes * ctx * H * 144          # compressed K+V bytes one layer's attention reads
+    attn_bytes = lanes * ctx * H * KV_BYTES[args.format]   # K+V bytes one layer's attention reads
     peak, peak_src = _peaks()
     achieved = attn_bytes / (call_ms / 1000.0) / 1e9
 
@@ -371,7 +374,7 @@ def run_gpu(args):
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (2-bit codes)", "data": "synthetic",
                 "config": _config({"ms_per_attention_call": call_ms, "peak_source": peak_src,
-                                   "step_calls": args.step_calls, "format": args.format}),
+                                   "step_calls": args.step_calls, "format": args.format}, args.format),
                 "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                              "frac": achieved / peak,
                              "traffic": _decode_traffic() if args.format == "hq2b" else None,
@@ -379,8 +382,9 @@ def run_gpu(args):
                                         if args.format == "hq2b" else
                                         ("paged_decode_attn (rotate_q_kernel + decode_hq2b_main<centred> + "
                                          "decode_hq2b_combine), one layer") if args.format == "hq2b_had" else
-                                        "paged_decode_attn (decode_hq2b_main<per-token K> + decode_hq2b_combine), "
-                                        "one layer"),
+                                        ("paged_decode_attn (decode_hq2b_main<per-token K> + decode_hq2b_combine), "
+                                         "one layer") if args.format == "hq2b_tok" else
+                                        "paged_decode_attn (decode_fp8_split + attn_combine), one layer"),
                              "algorithmic_bytes_per_launch": attn_bytes},
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -524,8 +528,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=WORKLOAD["ctx"])
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     ap.add_argument("--format", default="hq2b", choices=sorted(FORMATS),
-                    help="page format: hq2b (the benchmark's), hq2b_had (Walsh-Hadamard-rotated 2-bit) or "
-                         "hq2b_tok (K per token); the variants time decode only")
+                    help="page format: hq2b (the benchmark's), hq2b_had (Walsh-Hadamard-rotated 2-bit), "
+                         "hq2b_tok (K per token) or fp8 (E4M3); the variants time decode only")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-page-moves", action="store_true")
     ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],

@@ -12,6 +12,7 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
 struct AttnArgs;
 int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t stream);
 int launch_decode_hq2b(const AttnArgs& a, cudaStream_t stream);
+int launch_decode_fp8(const AttnArgs& a, cudaStream_t stream);
 int decode_split_tokens(int fmt);
 int prefill_split_tokens(int fmt);
 int decode_hq2b_slots(int max_seq_len);
@@ -32,8 +33,11 @@ constexpr float LOG2E = 1.4426950408889634f;
 int check_geom(const kvq_geom* g) {
   if (!g) return KVQ_ERR_INVALID_ARG;
   if (g->format != KVQ_FMT_HQ2B && g->format != KVQ_FMT_BF16 && g->format != KVQ_FMT_HQ2B_HAD &&
-      g->format != KVQ_FMT_HQ2B_TOK)
+      g->format != KVQ_FMT_HQ2B_TOK && g->format != KVQ_FMT_FP8)
     return KVQ_ERR_UNSUPPORTED;
+  if (g->format == KVQ_FMT_FP8 && (!(g->k_scale >= 0.0f && g->k_scale <= 3.0e38f) ||
+                                   !(g->v_scale >= 0.0f && g->v_scale <= 3.0e38f)))
+    return KVQ_ERR_INVALID_ARG;
   if (g->head_dim != D || g->page_tokens != P) return KVQ_ERR_UNSUPPORTED;
   if (g->num_layers <= 0 || g->num_kv_heads <= 0 || g->num_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
   if (g->num_layers > 4096 || g->num_kv_heads > 1024) return KVQ_ERR_UNSUPPORTED;
@@ -84,6 +88,8 @@ CacheView make_view(const kvq_geom* g, int layer, const void* pool, size_t pool_
   c.status = status;
   c.rotated = g->format == KVQ_FMT_HQ2B_HAD;
   c.ktok = g->format == KVQ_FMT_HQ2B_TOK;
+  c.k_scale = g->format == KVQ_FMT_FP8 && g->k_scale != 0.0f ? g->k_scale : 1.0f;
+  c.v_scale = g->format == KVQ_FMT_FP8 && g->v_scale != 0.0f ? g->v_scale : 1.0f;
   return c;
 }
 
@@ -212,6 +218,7 @@ int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t poo
                                         partial_bytes(lanes, g->num_q_heads, a.max_splits));
   }
   if (two_bit(g->format)) return launch_decode_hq2b(a, (cudaStream_t)stream);
+  if (g->format == KVQ_FMT_FP8) return launch_decode_fp8(a, (cudaStream_t)stream);
   return launch_attn_generic(g->format, a, 1, (cudaStream_t)stream);
 }
 

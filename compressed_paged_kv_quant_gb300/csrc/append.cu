@@ -69,6 +69,7 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
   if (max_new == 1) {
     dim3 g1(lanes, c.num_kv_heads);
     if (fmt == KVQ_FMT_HQ2B) append_one_kernel<KVQ_FMT_HQ2B><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
+    else if (fmt == KVQ_FMT_FP8) append_one_kernel<KVQ_FMT_FP8><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
     else append_one_kernel<KVQ_FMT_BF16><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
   } else if (fmt == KVQ_FMT_HQ2B) {
     if (!c.ktok) {   // the per-token-K format has no page close
@@ -79,7 +80,8 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
     append_rows_kernel<KVQ_FMT_HQ2B><<<gr, 256, 0, stream>>>(a);
   } else {
     dim3 gr((max_new + ROWS_PER_CTA - 1) / ROWS_PER_CTA, lanes);
-    append_rows_kernel<KVQ_FMT_BF16><<<gr, 256, 0, stream>>>(a);
+    if (fmt == KVQ_FMT_FP8) append_rows_kernel<KVQ_FMT_FP8><<<gr, 256, 0, stream>>>(a);
+    else append_rows_kernel<KVQ_FMT_BF16><<<gr, 256, 0, stream>>>(a);
   }
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -273,7 +273,7 @@ __device__ __forceinline__ void kclose_page(const AppendArgs& a, int b, int h, i
 }
 
 // One warp: token i of lane b, head h -- V row quantization (HQ2B; the K row too in the
-// per-token-K format) or plain stores (BF16), and the key into the ring (only the chunk's last 64 tokens: the ring keeps the newest key of each
+// per-token-K format), plain stores (BF16) or E4M3 conversion (FP8), and the key into the ring (only the chunk's last 64 tokens: the ring keeps the newest key of each
 // slot).  Returns after flagging when the token is past the table or its page is invalid.
 template <int FMT>
 __device__ __forceinline__ void append_row(const AppendArgs& a, int b, int h, int i, int start, int n, int off) {
@@ -303,6 +303,11 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, int b, int h, in
   if (FMT == KVQ_FMT_BF16) {
     reinterpret_cast<uint4*>(kblk + slot * D * 2)[lane] = kx;
     reinterpret_cast<uint4*>(vblk + slot * D * 2)[lane] = vx;
+    return;
+  }
+  if (FMT == KVQ_FMT_FP8) {
+    reinterpret_cast<uint2*>(kblk + slot * D)[lane] = fp8_encode8(kx, c.k_scale);
+    reinterpret_cast<uint2*>(vblk + slot * D)[lane] = fp8_encode8(vx, c.v_scale);
     return;
   }
   uint32_t packed, meta;

@@ -73,7 +73,9 @@ __global__ void __launch_bounds__(128) attn_split_generic(AttnArgs a, int decode
     const uint8_t* kblk = page + block_offset(FMT, H, c.layer, h, 0);
     const uint8_t* vblk = page + block_offset(FMT, H, c.layer, h, 1);
     float kx[8], vx[8];
-    if (FMT == KVQ_FMT_BF16 || t >= ef) {
+    if (FMT == KVQ_FMT_FP8) {
+      fp8_decode8(reinterpret_cast<const uint2*>(kblk + slot * D)[lane], c.k_scale, kx);
+    } else if (FMT == KVQ_FMT_BF16 || t >= ef) {
       const uint4 w = FMT == KVQ_FMT_BF16
                           ? reinterpret_cast<const uint4*>(kblk + slot * D * 2)[lane]
                           : reinterpret_cast<const uint4*>(c.ring + ring_row_offset(c, b, h, slot))[lane];
@@ -102,7 +104,9 @@ __global__ void __launch_bounds__(128) attn_split_generic(AttnArgs a, int decode
         kx[2 * j + 1] = sp.y * (float)(2 * (int)((codes >> (4 * j + 2)) & 3) - 3);
       }
     }
-    if (FMT == KVQ_FMT_BF16) {
+    if (FMT == KVQ_FMT_FP8) {
+      fp8_decode8(reinterpret_cast<const uint2*>(vblk + slot * D)[lane], c.v_scale, vx);
+    } else if (FMT == KVQ_FMT_BF16) {
       const uint4 w = reinterpret_cast<const uint4*>(vblk + slot * D * 2)[lane];
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -180,7 +184,9 @@ __global__ void __launch_bounds__(256) attn_combine(AttnArgs a, int decode, int 
   out[d] = den > 0.0f ? num / den : 0.0f;
 }
 
-int decode_split_tokens(int fmt) { return fmt == KVQ_FMT_HQ2B ? DECODE_SPLIT_HQ2B : GENERIC_SPLIT; }
+int decode_split_tokens(int fmt) {
+  return fmt == KVQ_FMT_HQ2B ? DECODE_SPLIT_HQ2B : fmt == KVQ_FMT_FP8 ? DECODE_SPLIT_FP8 : GENERIC_SPLIT;
+}
 int prefill_split_tokens(int) { return PREFILL_SPLIT; }
 
 int launch_attn_combine(const AttnArgs& a, int decode, cudaStream_t stream) {
@@ -196,6 +202,8 @@ int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t str
   dim3 grid(a.max_splits, (rows + warps - 1) / warps, a.lanes * a.c.num_kv_heads);
   if (fmt == KVQ_FMT_HQ2B)
     attn_split_generic<KVQ_FMT_HQ2B><<<grid, 32 * warps, 0, stream>>>(a, decode);
+  else if (fmt == KVQ_FMT_FP8)
+    attn_split_generic<KVQ_FMT_FP8><<<grid, 32 * warps, 0, stream>>>(a, decode);
   else
     attn_split_generic<KVQ_FMT_BF16><<<grid, 32 * warps, 0, stream>>>(a, decode);
   dim3 cg(a.lanes * rows, a.c.num_q_heads);

@@ -31,6 +31,7 @@
 #include "kvq_internal.cuh"
 #include "attn_args.cuh"
 #include "append_ops.cuh"
+#include "mma_tma.cuh"
 
 namespace kvq {
 
@@ -44,7 +45,6 @@ constexpr int DEC_PAIRS = KVQ_DEC_PAIRS;               // warp pairs per CTA
 constexpr int DEC_CTAS_PER_SM = KVQ_DEC_CTAS_PER_SM;  // resident CTAs per SM the grid is sized for
 constexpr int MIN_PAGES_PER_WARP = 2;
 constexpr int DEC_MAX_SLOTS = 96;            // partial records per (lane, query head), at most
-constexpr int SPIN_LIMIT = 1 << 16;          // bounded mbarrier waits (x ~1 us hint)
 
 // pages of lane b handled by the MMA path (everything before its exact tail)
 __device__ __forceinline__ int main_pages(const CacheView& c, const int32_t* seq_len, int b, bool* bad = nullptr) {
@@ -65,28 +65,8 @@ __device__ __forceinline__ int units_per_warp(int units, int nwarps, int min_wp)
 }
 
 // ----------------------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t y;
-  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
-
 __device__ __forceinline__ uint32_t h2mul(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-  __half2 r = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&r);
 }
 
@@ -133,41 +113,6 @@ __device__ __forceinline__ float fma_h15_f(uint16_t s, float c) {
 // lazy rescale: the running max of a head moves only when a page max exceeds it by more than
 // RESCALE_LOG2 (log2 domain), so P <= 2^0.5 and P * s_v stays below 65,504 for any finite V
 constexpr float RESCALE_LOG2 = 0.5f;
-
-// 2^x for the softmax (x <= 0 or -inf); one MUFU.EX2, relative error ~2^-22
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void tma_page(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// true once the barrier's phase with this parity completed; false after SPIN_LIMIT tries
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < SPIN_LIMIT; i++) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(1000u)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
 
 // Dims of word jw (16 dims) of thread column cq in the Q.K^T contraction.  The plain layout
 // gives each thread 64 contiguous dims; the per-token-K layout keeps every k-step inside one

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,14 +18,18 @@ constexpr int HQ2B_ROW = 64;       // bytes of 2-bit code per token row
 constexpr int HQ2B_BLOCK = 4608;   // 64 rows x 72 B: codes[64][64] + 512 B of scales / meta
 constexpr int HQ2B_META_OFF = 4096;
 constexpr int BF16_BLOCK = P * D * 2;  // 32,768 B
+constexpr int FP8_BLOCK = P * D;       // 16,384 B: one E4M3 byte per value
 constexpr int MAX_GROUP = 8;
 
 // split-K granularity of the generic attention kernel (tokens per split)
 constexpr int GENERIC_SPLIT = 1024;   // decode, generic kernel
 constexpr int DECODE_SPLIT_HQ2B = 1024;
+constexpr int DECODE_SPLIT_FP8 = 1024;    // tokens per CTA of the FP8 decode kernel
 constexpr int PREFILL_SPLIT = 8192;
 
-__host__ __device__ constexpr int block_bytes(int fmt) { return fmt == KVQ_FMT_BF16 ? BF16_BLOCK : HQ2B_BLOCK; }
+__host__ __device__ constexpr int block_bytes(int fmt) {
+  return fmt == KVQ_FMT_BF16 ? BF16_BLOCK : fmt == KVQ_FMT_FP8 ? FP8_BLOCK : HQ2B_BLOCK;
+}
 
 // Everything a kernel needs to address one layer of the cache.
 struct CacheView {
@@ -40,6 +45,7 @@ struct CacheView {
   int32_t* status;
   int rotated;                // KVQ_FMT_HQ2B_HAD: page rows hold Walsh-Hadamard-rotated K and V
   int ktok;                   // KVQ_FMT_HQ2B_TOK: K rows coded per token like V (no page close)
+  float k_scale, v_scale;     // KVQ_FMT_FP8: per-tensor scales (1 when the geometry gives 0)
 };
 
 __device__ __forceinline__ void flag(int32_t* status, int bits) {
@@ -68,6 +74,30 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 
 __device__ __forceinline__ float half_bits_to_float(uint16_t h) {
   return __half2float(__ushort_as_half(h));
+}
+
+// FP8 E4M3: eight bf16 values (one uint4) divided by `scale` in fp32 and converted with round to
+// nearest even, saturating at +-448 (one byte each, in order), and eight bytes back to floats
+// times `scale`.
+__device__ __forceinline__ uint2 fp8_encode8(uint4 w, float scale) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+  uint32_t h[4];
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const float2 f = make_float2(__fdiv_rn(bf16_lo(u[i]), scale), __fdiv_rn(bf16_hi(u[i]), scale));
+    h[i] = (uint32_t)__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+  }
+  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+__device__ __forceinline__ void fp8_decode8(uint2 b, float scale, float (&x)[8]) {
+  const uint32_t u[2] = {b.x, b.y};
+#pragma unroll
+  for (int i = 0; i < 4; i++) {
+    const __half2_raw r = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(u[i >> 1] >> (16 * (i & 1))), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&r));
+    x[2 * i] = f.x * scale;
+    x[2 * i + 1] = f.y * scale;
+  }
 }
 
 // In-place 256-point Walsh-Hadamard transform of one row held by a warp (lane l holds elements

@@ -18,6 +18,7 @@ FMT_HQ2B = 0
 FMT_BF16 = 1
 FMT_HQ2B_HAD = 2   # the HQ2B layout over Walsh-Hadamard-rotated K and V rows
 FMT_HQ2B_TOK = 3   # the HQ2B layout with K rows coded per token (V rule), no page close
+FMT_FP8 = 4        # K and V rows as FP8 E4M3 with a per-tensor scale each
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -49,7 +50,8 @@ class KvqError(RuntimeError):
 class Geom(ctypes.Structure):
     _fields_ = [("format", ctypes.c_int32), ("num_layers", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("k_scale", ctypes.c_float), ("v_scale", ctypes.c_float)]
 
     def __repr__(self):
         return (f"Geom(format={self.format}, L={self.num_layers}, Hkv={self.num_kv_heads}, "
@@ -57,8 +59,9 @@ class Geom(ctypes.Structure):
 
 
 def geom(fmt: int, num_layers: int, num_kv_heads: int, num_q_heads: int,
-         head_dim: int = 256, page_tokens: int = 64) -> Geom:
-    return Geom(fmt, num_layers, num_kv_heads, num_q_heads, head_dim, page_tokens)
+         head_dim: int = 256, page_tokens: int = 64, k_scale: float = 0.0, v_scale: float = 0.0) -> Geom:
+    """k_scale / v_scale: the FP8 format's per-tensor scales (0 means 1)."""
+    return Geom(fmt, num_layers, num_kv_heads, num_q_heads, head_dim, page_tokens, k_scale, v_scale)
 
 
 _lib = None

@@ -60,7 +60,15 @@ typedef struct CUstream_st* kvq_stream_t; /* same handle as cudaStream_t; NULL =
  * exact; a key is read from it only inside the window (t >= seq_len - window), so with window 0
  * every key, the open page's included, comes from its codes.  All calls take it; prefill runs
  * on the CUDA-core split kernel. */
-typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_HQ2B_HAD = 2, KVQ_FMT_HQ2B_TOK = 3 } kvq_format;
+/* KVQ_FMT_FP8: K and V rows as OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, largest finite 448, no infinity), one byte per value: a (layer, head, K or V) block of a
+ * page is 64 rows x 256 B = 16,384 B, half of BF16 -- the FP8 cache of the vLLM study quoted in
+ * "Half the Cache, Twice the Context" ("What the vendors actually measured").  Append stores
+ * E4M3(x / scale) with x / scale in fp32, rounded to nearest even and saturated at +-448; reads
+ * decode the byte and multiply by the scale (kvq_geom.k_scale / v_scale, 0 meaning 1).  No
+ * ring (ring may be NULL, ring bytes are 0) and no window: every key comes from its page. */
+typedef enum { KVQ_FMT_HQ2B = 0, KVQ_FMT_BF16 = 1, KVQ_FMT_HQ2B_HAD = 2, KVQ_FMT_HQ2B_TOK = 3,
+               KVQ_FMT_FP8 = 4 } kvq_format;
 
 typedef struct {
   int32_t format;       /* kvq_format */
@@ -69,6 +77,8 @@ typedef struct {
   int32_t num_q_heads;  /* multiple of num_kv_heads, group <= 8 */
   int32_t head_dim;     /* must be 256 */
   int32_t page_tokens;  /* must be 64 */
+  float k_scale;        /* KVQ_FMT_FP8: per-tensor scale of K (0 means 1; else finite, > 0) */
+  float v_scale;        /* KVQ_FMT_FP8: per-tensor scale of V; other formats ignore both */
 } kvq_geom;
 
 /* host-side return codes */

@@ -60,6 +60,19 @@ def test_two_bit_variants_share_the_layout(L):
     assert kvq.decode_workspace_bytes(kvq.geom(kvq.FMT_HQ2B_HAD, 16, 4, 24), 8, 40960) == base + 8 * 24 * 512
 
 
+def test_fp8_sizes_and_scales(L):
+    """FP8 E4M3 pages: 256 B per head per token for K and for V, no ring; a negative or
+    non-finite scale is refused."""
+    g = kvq.geom(kvq.FMT_FP8, 16, 4, 24)
+    assert kvq.token_bytes(g) == 16 * 4 * 2 * 256
+    assert kvq.page_bytes(g) == 64 * 16 * 4 * 2 * 256
+    assert kvq.ring_bytes(g, 8) == 0
+    assert kvq.page_bytes(kvq.geom(kvq.FMT_FP8, 16, 4, 24, k_scale=0.5, v_scale=2.0)) == kvq.page_bytes(g)
+    for bad in (-1.0, float("inf"), float("nan")):
+        assert kvq.page_bytes(kvq.geom(kvq.FMT_FP8, 16, 4, 24, k_scale=bad)) == 0
+        assert kvq.page_bytes(kvq.geom(kvq.FMT_FP8, 16, 4, 24, v_scale=bad)) == 0
+
+
 @pytest.mark.parametrize("bad", [dict(head_dim=128), dict(page_tokens=32), dict(format=7),
                                  dict(num_q_heads=36), dict(num_q_heads=10)])
 def test_unsupported_geometry_is_refused(L, bad):

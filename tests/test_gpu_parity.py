@@ -10,7 +10,7 @@ from oracle_side import assert_close, host_kv
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-HQ, BF, HAD, TOK = oracle.FMT_HQ2B, oracle.FMT_BF16, oracle.FMT_HQ2B_HAD, oracle.FMT_HQ2B_TOK
+HQ, BF, HAD, TOK, FP8 = oracle.FMT_HQ2B, oracle.FMT_BF16, oracle.FMT_HQ2B_HAD, oracle.FMT_HQ2B_TOK, oracle.FMT_FP8
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -21,9 +21,9 @@ def _lib():
     build.build()
 
 
-def _dw(wl, fmt, fill=0xA5):
+def _dw(wl, fmt, fill=0xA5, scales=(0.0, 0.0)):
     from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
-    return DeviceWorkload(wl, fmt, "cuda", fill)
+    return DeviceWorkload(wl, fmt, "cuda", fill, k_scale=scales[0], v_scale=scales[1])
 
 
 def _u16(t):
@@ -46,9 +46,9 @@ def _custom(lens, L=1, H=1, Hq=4, seed=0, window=0, extra_pages=3, k_out=True, v
                           k_outliers=k_out, v_outliers=v_out)
 
 
-def _oracle_full(wl, fmt, layers=None, fill=0xA5):
+def _oracle_full(wl, fmt, layers=None, fill=0xA5, scales=(0.0, 0.0)):
     """Oracle pool/ring with the workload's own geometry and page table, every lane filled."""
-    g = oracle.geom(fmt, wl.num_layers, wl.num_kv_heads, wl.num_q_heads)
+    g = oracle.geom(fmt, wl.num_layers, wl.num_kv_heads, wl.num_q_heads, *scales)
     pool = np.full(wl.pool_pages * oracle.page_bytes(g), fill, np.uint8)
     ring = np.zeros((wl.lanes, wl.num_layers, wl.num_kv_heads, 64, 256), np.uint16)
     for layer in (range(wl.num_layers) if layers is None else layers):
@@ -155,6 +155,33 @@ def test_per_token_k_append_bytes(chunking):
     np.testing.assert_array_equal(_u16(dw.cache.ring), ring.ravel())
 
 
+@pytest.mark.parametrize("chunking,scales", [("one", (0.0, 0.0)), ("random", (0.0, 0.0)), ("random", (0.25, 3.0))])
+def test_fp8_append_bytes(chunking, scales):
+    """The FP8 E4M3 format: every page byte equals the oracle's E4M3 of x / scale."""
+    wl = _custom([300, 129, 64, 5], L=2, H=2, Hq=4)
+    dw = _dw(wl, FP8, scales=scales)
+    _gpu_fill(dw, chunking)
+    assert dw.cache.read_status() == 0
+    g, pool, _ = _oracle_full(wl, FP8, scales=scales)
+    np.testing.assert_array_equal(dw.cache.pool.cpu().numpy(), pool)
+
+
+@pytest.mark.parametrize("scales", [(0.0, 0.0), (0.25, 3.0)])
+def test_fp8_decode_with_scales(scales):
+    wl = _custom(LENS, L=1, H=2, Hq=12)
+    dw = _dw(wl, FP8, scales=scales)
+    _gpu_fill(dw)
+    g, pool, _ = _oracle_full(wl, FP8, scales=scales)
+    ws, out = dw.decode_buffers()
+    ws.view(torch.int32).fill_(0x7FC00001)
+    dw.decode(0, dw.step_q(0), ws, out)
+    qh = np.concatenate([wl.q_np(0, b, n - 1, 1) for b, n in enumerate(LENS)])
+    ref, st = oracle.decode(g, 0, pool, None, 0, wl.page_table, wl.lanes, LENS, qh, dw.sm_scale)
+    assert st == 0
+    assert_close(out.cpu().numpy(), ref, what=f"fp8 decode scales={scales}")
+    assert dw.cache.read_status() == 0
+
+
 def test_rotated_format_refuses_prefill():
     from compressed_paged_kv_quant_gb300 import kvq
     wl = _custom([128], L=1, H=1, Hq=4)
@@ -177,7 +204,7 @@ LENS = [1, 63, 64, 65, 700, 1500, 2049, 3000]
 
 
 @pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (HQ, 17), (BF, 0), (HAD, 0), (HAD, 64), (HAD, 17),
-                                        (TOK, 0), (TOK, 64), (TOK, 17)])
+                                        (TOK, 0), (TOK, 64), (TOK, 17), (FP8, 0)])
 def test_decode_ragged_lanes(fmt, window):
     wl = _custom(LENS, L=2, H=2, Hq=12, window=window)
     dw = _dw(wl, fmt)
@@ -189,7 +216,7 @@ def test_decode_ragged_lanes(fmt, window):
         q = dw.step_q(layer)
         dw.decode(layer, q, ws, out)
         qh = np.concatenate([wl.q_np(layer, b, n - 1, 1) for b, n in enumerate(LENS)])
-        ref, st = oracle.decode(g, layer, pool, ring if fmt != BF else None, window, wl.page_table, wl.lanes,
+        ref, st = oracle.decode(g, layer, pool, ring if fmt not in (BF, FP8) else None, window, wl.page_table, wl.lanes,
                                 LENS, qh, dw.sm_scale)
         assert st == 0
         assert_close(out.cpu().numpy(), ref, what=f"decode fmt={fmt} W={window} layer={layer}")
@@ -223,7 +250,7 @@ def test_decode_zero_length_lane_gives_zeros():
     assert torch.all(torch.isfinite(out))
 
 
-@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (BF, 0), (TOK, 0), (TOK, 64)])
+@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (BF, 0), (TOK, 0), (TOK, 64), (FP8, 0)])
 def test_prefill_chunks(fmt, window):
     """Causal chunks over a compressed prefix: (prefix, chunk) = (300, 100), (0, 70), (1000, 1100)."""
     prefix, chunk = [300, 0, 1000], [100, 70, 1100]
@@ -240,7 +267,7 @@ def test_prefill_chunks(fmt, window):
         q = torch.cat([wl.q_torch(layer, b, prefix[b], chunk[b], "cuda") for b in range(3)])
         dw.prefill(layer, q, prefix, chunk, offs, ws, out)
         qh = np.concatenate([wl.q_np(layer, b, prefix[b], chunk[b]) for b in range(3)])
-        ref, st = oracle.prefill(g, layer, pool, ring if fmt != BF else None, window, wl.page_table, 3, prefix,
+        ref, st = oracle.prefill(g, layer, pool, ring if fmt not in (BF, FP8) else None, window, wl.page_table, 3, prefix,
                                  chunk, offs, lens, qh, dw.sm_scale)
         assert st == 0
         assert_close(out.cpu().numpy(), ref, what=f"prefill fmt={fmt} W={window} layer={layer}")
