@@ -7,7 +7,7 @@
 //
 // CTA = 4 warps = one (lane, KV head, split of F8_SPLIT tokens).  A page's K and V blocks of
 // this layer and head are adjacent in the page (16 KB each), so one 1-D bulk copy
-// (cp.async.bulk) moves both into a 2-stage shared-memory ring; every wait is bounded.  Warp w
+// (cp.async.bulk) moves both into a F8_STAGES-deep shared-memory ring; every wait is bounded.  Warp w
 // takes tokens 16w .. 16w + 15 of every page and runs its own online softmax over them:
 //   S = K^ . q^T on mma.sync m16n8k16 (fp16 in, fp32 accumulate): A = K bytes turned into fp16
 //     pairs by one cvt.e4m3x2 each (E4M3 -> fp16 is exact), B = q (fp16) of the group's heads
@@ -27,12 +27,19 @@
 
 namespace kvq {
 
+#ifndef KVQ_F8_STAGES
+#define KVQ_F8_STAGES 2
+#endif
+#ifndef KVQ_F8_CTAS
+#define KVQ_F8_CTAS 3
+#endif
 constexpr int F8_WARPS = 4;
-constexpr int F8_STAGES = 2;
+constexpr int F8_STAGES = KVQ_F8_STAGES;        // pages in the shared-memory ring
+constexpr int F8_CTAS = KVQ_F8_CTAS;            // resident CTAs per SM the launch bounds ask for
 constexpr int F8_STAGE_BYTES = 2 * FP8_BLOCK;                 // K block + V block: 32 KB
-constexpr int F8_Q_OFF = F8_STAGES * F8_STAGE_BYTES;          // q, fp16 [8 heads][256]
-constexpr int F8_BAR_OFF = F8_Q_OFF + MAX_GROUP * D * 2;      // full[2], empty[2], valid[2]
-constexpr int F8_SMEM = F8_BAR_OFF + 64;
+constexpr int F8_Q_OFF = F8_STAGES * F8_STAGE_BYTES;          // q as B fragments: [8][32 lanes] uint4
+constexpr int F8_BAR_OFF = F8_Q_OFF + MAX_GROUP * D * 2;      // full[S], empty[S], valid[S]
+constexpr int F8_SMEM = F8_BAR_OFF + F8_STAGES * 20 + 16;
 constexpr float F8_LAZY = 0.5f;   // lazy rescale: a head's max moves only past +0.5 (log2), P <= 2^0.5
 
 // two E4M3 bytes (low 16 bits) -> fp16 pair, exact
@@ -43,7 +50,7 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t x) {
 }
 
 // grid (lanes * H, splits); 128 threads
-__global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a) {
+__global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
@@ -60,11 +67,11 @@ __global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a)
   const int p0 = t0 / P, np = (t1 - t0 + P - 1) / P;
 
   uint8_t* stage = smem;
-  __half* qs = reinterpret_cast<__half*>(smem + F8_Q_OFF);
+  uint4* qf = reinterpret_cast<uint4*>(smem + F8_Q_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + F8_BAR_OFF);
-  volatile int* svalid = reinterpret_cast<volatile int*>(smem + F8_BAR_OFF + 32);
+  volatile int* svalid = reinterpret_cast<volatile int*>(smem + F8_BAR_OFF + 16 * F8_STAGES);
   auto FULL = [&](int i) { return smem_u32(&bars[i]); };
-  auto EMPTY = [&](int i) { return smem_u32(&bars[2 + i]); };
+  auto EMPTY = [&](int i) { return smem_u32(&bars[F8_STAGES + i]); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < F8_STAGES; i++) {
@@ -73,23 +80,23 @@ __global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a)
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  // q of the group's heads (rows >= G are zero) as fp16
-  for (int i = threadIdx.x; i < MAX_GROUP * D / 8; i += blockDim.x) {
-    const int hd = i / (D / 8), d8 = i % (D / 8);
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (hd < G) w = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + hd) * D)[d8];
-    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-    uint32_t o[4];
+  // q of head g of the group (zero past G) as this lane's fp16 B fragments: dims 64cq + 8k .. + 7
+  // in qf[k * 32 + lane], k = 0..7, so the loop's reads are lane-contiguous (no bank conflicts)
+  if (warp == 0) {
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const __half2 p = __floats2half2_rn(bf16_lo(u[j]), bf16_hi(u[j]));
-      o[j] = *reinterpret_cast<const uint32_t*>(&p);
+    for (int k = 0; k < 8; k++) {
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G) w = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + g) * D + 64 * cq)[k];
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; j++) o[j] = pack_h2(bf16_lo(u[j]), bf16_hi(u[j]));
+      qf[k * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    reinterpret_cast<uint4*>(qs)[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
   __syncthreads();
 
-  // page j of the split into stage j % 2 (thread 0 only)
+  // page j of the split into stage j % F8_STAGES (thread 0 only)
   int issued = 0;
   auto issue = [&](int j) {
     const int st = j % F8_STAGES;
@@ -106,10 +113,8 @@ __global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a)
     }
     issued = j + 1;
   };
-  if (threadIdx.x == 0) {
-    issue(0);
-    if (np > 1) issue(1);
-  }
+  if (threadIdx.x == 0)
+    for (int j = 0; j < F8_STAGES && j < np; j++) issue(j);
 
   const float kscale = a.scale_log2 * c.k_scale;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2cq, 2cq+1
@@ -119,7 +124,6 @@ __global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a)
 #pragma unroll
     for (int e = 0; e < 4; e++) O[i][e] = 0.f;
   bool timed_out = false;
-  const uint8_t* qrow = reinterpret_cast<const uint8_t*>(qs) + g * (D * 2) + 64 * cq * 2;
   for (int j = 0; j < np; j++) {
     const int st = j % F8_STAGES;
     const uint32_t par = (j / F8_STAGES) & 1;
@@ -139,8 +143,7 @@ __global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a)
       for (int c4 = 0; c4 < 4; c4++) {
         const uint4 ka = *reinterpret_cast<const uint4*>(krA + 16 * c4);
         const uint4 kbw = *reinterpret_cast<const uint4*>(krB + 16 * c4);
-        const uint4 q0 = *reinterpret_cast<const uint4*>(qrow + 32 * c4);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(qrow + 32 * c4 + 16);
+        const uint4 q0 = qf[(2 * c4) * 32 + lane], q1 = qf[(2 * c4 + 1) * 32 + lane];
         const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kbw.x, kbw.y, kbw.z, kbw.w};
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
@@ -204,7 +207,7 @@ __global__ void __launch_bounds__(F8_WARPS * 32, 3) decode_fp8_split(AttnArgs a)
     }
     __syncwarp();
     if (lane == 0) asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(EMPTY(st)) : "memory");
-    // refill this stage with page j + 2 once all four warps have released it
+    // refill this stage with page j + F8_STAGES once all four warps have released it
     if (threadIdx.x == 0 && j + F8_STAGES < np) {
       if (mbar_wait(EMPTY(st), par)) issue(j + F8_STAGES);
       else timed_out = true;
