@@ -47,7 +47,7 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-DECODE_SOURCES = ("decode_hq2b.cu", "kvq_internal.cuh", "attn_args.cuh", "append_ops.cuh")
+DECODE_SOURCES = ("decode_hq2b.cu", "kvq_internal.cuh", "attn_args.cuh", "append_ops.cuh", "mma_tma.cuh")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_hq2b_main_27b_8x40960.md")
 
 
