@@ -6,18 +6,22 @@
 // format, so this kernel is built to stream pages at HBM rate with little work per byte.
 //
 // CTA = 4 warps = one (lane, KV head, split of F8_SPLIT tokens).  A page's K and V blocks of
-// this layer and head are adjacent in the page (16 KB each), so one 1-D bulk copy
-// (cp.async.bulk) moves both into a F8_STAGES-deep shared-memory ring; every wait is bounded.  Warp w
-// takes tokens 16w .. 16w + 15 of every page and runs its own online softmax over them:
+// this layer and head (16 KB each, adjacent in the page) are copied by all 128 threads with
+// 16 B cp.async into a F8_STAGES-deep shared-memory ring whose rows are padded from 256 to
+// 272 B: with the fragment ownership below, every 16 B shared-memory read of a warp then hits
+// eight different bank groups (unpadded rows 256 B apart put K reads 2-way and V reads 4-way
+// in conflict).  Completion is an mbarrier of 128 cp.async arrivals; every wait is bounded.
+// Warp w takes tokens 16w .. 16w + 15 of every page and runs its own online softmax over them:
 //   S = K^ . q^T on mma.sync m16n8k16 (fp16 in, fp32 accumulate): A = K bytes turned into fp16
 //     pairs by one cvt.e4m3x2 each (E4M3 -> fp16 is exact), B = q (fp16) of the group's heads
 //     (padded to 8).  The contraction order over the 256 dims is permuted so that a thread's A
-//     bytes of a k-step are one 32-bit word of its token row; a dot product does not depend
-//     on its order.  The K scale multiplies the fp32 score.
+//     bytes of a k-step are one 32-bit word of its token row (thread column cq reads 16 B chunks
+//     2cq + 8(c4 & 1) + (c4 >> 1), c4 = 0..3); a dot product does not depend on its order.  The
+//     K scale multiplies the fp32 score.
 //   O^T += V^ . P^T on the same MMA: A = V bytes of two tokens per fp16 pair (one byte permute,
 //     two cvt), B = P (fp16, P <= 2^0.5 under the lazy rescale) moved from the S accumulator
-//     layout to the B layout with movmatrix.trans.  Rows of O^T are dims in the order
-//     32 g + 2 j (+1) for thread row g, so a thread's V bytes are 32 contiguous bytes a token.
+//     layout to the B layout with movmatrix.trans.  Rows of O^T are dims: thread row g owns
+//     dims 128 hh + 16 g + 0..15 (hh = 0, 1), 16 contiguous bytes of a token row per hh.
 // At the end the 4 warps' (m, l, O) merge in FP32 in shared memory, times the V scale, into
 // one partial record of the split; the log-sum-exp combine (attn_generic.cu) merges splits --
 // the two-level accumulation of "Half the Cache", "The cliff is in the accumulator".
@@ -36,11 +40,19 @@ namespace kvq {
 constexpr int F8_WARPS = 4;
 constexpr int F8_STAGES = KVQ_F8_STAGES;        // pages in the shared-memory ring
 constexpr int F8_CTAS = KVQ_F8_CTAS;            // resident CTAs per SM the launch bounds ask for
-constexpr int F8_STAGE_BYTES = 2 * FP8_BLOCK;                 // K block + V block: 32 KB
+constexpr int F8_ROW = D + 16;                                // a padded 256 B page row
+constexpr int F8_STAGE_BYTES = 2 * P * F8_ROW;                // K rows then V rows: 34,816 B
 constexpr int F8_Q_OFF = F8_STAGES * F8_STAGE_BYTES;          // q as B fragments: [8][32 lanes] uint4
-constexpr int F8_BAR_OFF = F8_Q_OFF + MAX_GROUP * D * 2;      // full[S], empty[S], valid[S]
-constexpr int F8_SMEM = F8_BAR_OFF + F8_STAGES * 20 + 16;
+constexpr int F8_BAR_OFF = F8_Q_OFF + MAX_GROUP * D * 2;      // full[S]
+constexpr int F8_SMEM = F8_BAR_OFF + F8_STAGES * 8;
 constexpr float F8_LAZY = 0.5f;   // lazy rescale: a head's max moves only past +0.5 (log2), P <= 2^0.5
+
+// 16 B chunk of thread column cq for k-step group c4 (conflict-free K reads, see above)
+__device__ __forceinline__ int f8_kchunk(int cq, int c4) { return 2 * cq + 8 * (c4 & 1) + (c4 >> 1); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
 
 // two E4M3 bytes (low 16 bits) -> fp16 pair, exact
 __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t x) {
@@ -69,24 +81,21 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
   uint8_t* stage = smem;
   uint4* qf = reinterpret_cast<uint4*>(smem + F8_Q_OFF);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + F8_BAR_OFF);
-  volatile int* svalid = reinterpret_cast<volatile int*>(smem + F8_BAR_OFF + 16 * F8_STAGES);
   auto FULL = [&](int i) { return smem_u32(&bars[i]); };
-  auto EMPTY = [&](int i) { return smem_u32(&bars[F8_STAGES + i]); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < F8_STAGES; i++) {
-      mbar_init(FULL(i), 1);
-      mbar_init(EMPTY(i), F8_WARPS);
-    }
+    for (int i = 0; i < F8_STAGES; i++) mbar_init(FULL(i), F8_WARPS * 32);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  // q of head g of the group (zero past G) as this lane's fp16 B fragments: dims 64cq + 8k .. + 7
-  // in qf[k * 32 + lane], k = 0..7, so the loop's reads are lane-contiguous (no bank conflicts)
+  // q of head g of the group (zero past G) as this lane's fp16 B fragments: dims
+  // 16 f8_kchunk(cq, k / 2) + 8 (k & 1) .. + 7 in qf[k * 32 + lane], k = 0..7, so the loop's reads
+  // are lane-contiguous (no bank conflicts)
   if (warp == 0) {
 #pragma unroll
     for (int k = 0; k < 8; k++) {
       uint4 w = make_uint4(0u, 0u, 0u, 0u);
-      if (g < G) w = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + g) * D + 64 * cq)[k];
+      if (g < G)
+        w = reinterpret_cast<const uint4*>(a.q + ((int64_t)b * Hq + h * G + g) * D)[2 * f8_kchunk(cq, k >> 1) + (k & 1)];
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
       uint32_t o[4];
 #pragma unroll
@@ -96,25 +105,30 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
   }
   __syncthreads();
 
-  // page j of the split into stage j % F8_STAGES (thread 0 only)
-  int issued = 0;
+  // page j of the split into stage j % F8_STAGES, by every thread: 16 B chunk q = thread + 128 i of
+  // the page's 2,048 (K block then V block) to row q / 16, column q % 16 of the padded ring
+  uint32_t valid = 0;   // bit per stage: the page is in the pool (same in every thread)
   auto issue = [&](int j) {
     const int st = j % F8_STAGES;
     const int32_t phys = c.page_table[(int64_t)b * c.max_pages + p0 + j];
     const bool ok = phys >= 0 && phys < c.pool_pages;
-    svalid[st] = ok ? 1 : 0;
+    valid = ok ? (valid | (1u << st)) : (valid & ~(1u << st));
     if (ok) {
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_FP8, H, c.layer, h, 0);
-      tma_page(smem_u32(stage + st * F8_STAGE_BYTES), src, F8_STAGE_BYTES, FULL(st));
+      const uint32_t dst = smem_u32(stage + st * F8_STAGE_BYTES);
+#pragma unroll 4
+      for (int i = 0; i < 2 * FP8_BLOCK / 16 / (F8_WARPS * 32); i++) {
+        const int q = threadIdx.x + F8_WARPS * 32 * i;
+        cp_async16(dst + (q >> 4) * F8_ROW + 16 * (q & 15), src + 16 * q);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(FULL(st)) : "memory");
     } else {
-      flag(c.status, KVQ_STATUS_PAGE_OOB);
+      if (threadIdx.x == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
       asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(FULL(st)) : "memory");
     }
-    issued = j + 1;
   };
-  if (threadIdx.x == 0)
-    for (int j = 0; j < F8_STAGES && j < np; j++) issue(j);
+  __syncthreads();   // barrier initialisation visible to every thread
+  for (int j = 0; j < F8_STAGES && j < np; j++) issue(j);
 
   const float kscale = a.scale_log2 * c.k_scale;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // heads 2cq, 2cq+1
@@ -127,22 +141,23 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
   for (int j = 0; j < np; j++) {
     const int st = j % F8_STAGES;
     const uint32_t par = (j / F8_STAGES) & 1;
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(FULL(st), par))) {
+    if (__syncthreads_or(!mbar_wait(FULL(st), par))) {   // every thread leaves together
       timed_out = true;
       break;
     }
-    if (svalid[st]) {
+    if (valid & (1u << st)) {
       const uint8_t* kb = stage + st * F8_STAGE_BYTES;
-      const uint8_t* vb = kb + FP8_BLOCK;
-      // ---- S = K^ . q^T for tokens 16 warp + g (+8); thread column cq owns dims 64cq .. 64cq+63,
-      // k-step 4 c4 + i covering dims 64cq + 16c4 + 4i + {0,1} (A regs 0/1) and {2,3} (regs 2/3)
-      const uint8_t* krA = kb + (16 * warp + g) * D + 64 * cq;
-      const uint8_t* krB = krA + 8 * D;
+      const uint8_t* vb = kb + P * F8_ROW;
+      // ---- S = K^ . q^T for tokens 16 warp + g (+8); k-step 4 c4 + i of thread column cq covers
+      // dims 16 f + 4i + {0,1} (A regs 0/1) and {2,3} (regs 2/3), f = f8_kchunk(cq, c4)
+      const uint8_t* krA = kb + (16 * warp + g) * F8_ROW;
+      const uint8_t* krB = krA + 8 * F8_ROW;
       float S[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; c4++) {
-        const uint4 ka = *reinterpret_cast<const uint4*>(krA + 16 * c4);
-        const uint4 kbw = *reinterpret_cast<const uint4*>(krB + 16 * c4);
+        const int f = f8_kchunk(cq, c4);
+        const uint4 ka = *reinterpret_cast<const uint4*>(krA + 16 * f);
+        const uint4 kbw = *reinterpret_cast<const uint4*>(krB + 16 * f);
         const uint4 q0 = qf[(2 * c4) * 32 + lane], q1 = qf[(2 * c4 + 1) * 32 + lane];
         const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kbw.x, kbw.y, kbw.z, kbw.w};
         const uint32_t qw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
@@ -185,18 +200,19 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
       l1 += pb + pd;
       // P as the B operand (k = token, n = head): transpose the accumulator's 8x8 halves
       const uint32_t b0 = movmatrix_t(pack_h2(pa, pb)), b1 = movmatrix_t(pack_h2(pc, pd));
-      // ---- O^T += V^ . P^T; thread row g owns dims 32g .. 32g+31, tokens 2cq, 2cq+1, 2cq+8, 2cq+9
-      const uint8_t* vr = vb + (16 * warp + 2 * cq) * D + 32 * g;
+      // ---- O^T += V^ . P^T; thread row g owns dims 128 hh + 16g + 0..15, tokens 2cq, 2cq+1,
+      // 2cq+8, 2cq+9
+      const uint8_t* vr = vb + (16 * warp + 2 * cq) * F8_ROW + 16 * g;
 #pragma unroll
       for (int hh = 0; hh < 2; hh++) {
-        const uint4 r0 = *reinterpret_cast<const uint4*>(vr + 16 * hh);
-        const uint4 r1 = *reinterpret_cast<const uint4*>(vr + D + 16 * hh);
-        const uint4 r2 = *reinterpret_cast<const uint4*>(vr + 8 * D + 16 * hh);
-        const uint4 r3 = *reinterpret_cast<const uint4*>(vr + 9 * D + 16 * hh);
+        const uint4 r0 = *reinterpret_cast<const uint4*>(vr + 128 * hh);
+        const uint4 r1 = *reinterpret_cast<const uint4*>(vr + F8_ROW + 128 * hh);
+        const uint4 r2 = *reinterpret_cast<const uint4*>(vr + 8 * F8_ROW + 128 * hh);
+        const uint4 r3 = *reinterpret_cast<const uint4*>(vr + 9 * F8_ROW + 128 * hh);
         const uint32_t w0[4] = {r0.x, r0.y, r0.z, r0.w}, w1[4] = {r1.x, r1.y, r1.z, r1.w};
         const uint32_t w2[4] = {r2.x, r2.y, r2.z, r2.w}, w3[4] = {r3.x, r3.y, r3.z, r3.w};
 #pragma unroll
-        for (int dj = 0; dj < 8; dj++) {      // dims 32g + 16hh + 2dj, +1
+        for (int dj = 0; dj < 8; dj++) {      // dims 128hh + 16g + 2dj, +1
           const uint32_t sel = (dj & 1) ? 0x7362u : 0x5140u;
           const uint32_t lo = __byte_perm(w0[dj >> 1], w1[dj >> 1], sel);   // tokens 2cq, 2cq+1
           const uint32_t hi = __byte_perm(w2[dj >> 1], w3[dj >> 1], sel);   // tokens 2cq+8, 2cq+9
@@ -205,24 +221,15 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(EMPTY(st)) : "memory");
-    // refill this stage with page j + F8_STAGES once all four warps have released it
-    if (threadIdx.x == 0 && j + F8_STAGES < np) {
-      if (mbar_wait(EMPTY(st), par)) issue(j + F8_STAGES);
-      else timed_out = true;
-    }
-    if (warp == 0 && __shfl_sync(0xFFFFFFFFu, (int)timed_out, 0)) {
-      timed_out = true;
-      break;
-    }
+    // every warp is done with this stage: refill it with page j + F8_STAGES
+    __syncthreads();
+    if (j + F8_STAGES < np) issue(j + F8_STAGES);
   }
-  if (timed_out && lane == 0) flag(c.status, KVQ_STATUS_TIMEOUT);
-  // copies still in flight must land before the stages are reused (bounded waits)
-  if (threadIdx.x == 0)
-    for (int j = max(0, issued - F8_STAGES); j < issued; j++) mbar_wait(FULL(j % F8_STAGES), (j / F8_STAGES) & 1);
+  if (timed_out && threadIdx.x == 0) flag(c.status, KVQ_STATUS_TIMEOUT);
+  // this thread's copies still in flight land before the stages are reused or the CTA exits
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
   __syncthreads();
-  if (__syncthreads_or(timed_out)) return;   // the status word reports it; no partial is written
+  if (timed_out) return;   // (uniform) the status word reports it; no partial is written
 
   // ---- merge the 4 warps: per head the largest m, weights 2^(m_w - m), O and l summed in FP32
 #pragma unroll
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
   for (int i = 0; i < 16; i++)
 #pragma unroll
     for (int e = 0; e < 4; e++) {
-      const int head = 2 * cq + (e & 1), dim = 32 * g + 2 * i + (e >> 1);
+      const int head = 2 * cq + (e & 1), dim = 128 * (i >> 3) + 16 * g + 2 * (i & 7) + (e >> 1);
       sm_o[(warp * MAX_GROUP + head) * D + dim] = O[i][e] * wt[e & 1];
     }
   __syncthreads();
@@ -287,6 +294,7 @@ int launch_decode_fp8(const AttnArgs& a, cudaStream_t stream) {
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
     cudaFuncSetAttribute(decode_fp8_split, cudaFuncAttributeMaxDynamicSharedMemorySize, F8_SMEM);
+    cudaFuncSetAttribute(decode_fp8_split, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     attr_set[dev] = true;
   }
   const int splits = (int)((a.max_seq_len + a.split_tokens - 1) / a.split_tokens);
