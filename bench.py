@@ -52,11 +52,17 @@ DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_hq2b_main_27b_8x40960.md
 
 
 def _decode_source_hash():
+    """sha256 of the decode kernel's sources with // comments and blank lines dropped, so that an
+    edit of comments alone keeps a profile's counters valid."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "compressed_paged_kv_quant_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "compressed_paged_kv_quant_gb300", "csrc", name)) as f:
+            for line in f:
+                code = re.sub(r"//.*", "", line).rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()
 
 

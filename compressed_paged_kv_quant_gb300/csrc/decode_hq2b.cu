@@ -7,27 +7,30 @@
 //
 // Work split.  Every (lane, KV head) contributes the pages before its exact tail (the open
 // page and the recent-key window, handled by the combine kernel).  All those pages form one
-// list ordered (lane, head, page); a persistent grid of 2 CTAs x 4 warps per SM cuts it into
-// equal contiguous ranges, one per warp, so ragged lanes cost nothing in balance.  A warp
-// writes one FP32 partial (m, l, acc[256]) for each (lane, head) segment its range touches.
+// list ordered (lane, head, page); a persistent grid of 2 CTAs per SM, each of DEC_PAIRS warp
+// pairs, cuts it into equal contiguous ranges, one per pair, so ragged lanes cost nothing in
+// balance.  A pair writes one FP32 partial (m, l, acc[256]) for each (lane, head) segment its
+// range touches; decode_hq2b_combine merges them with the tail.
 //
-// Per warp, pages stream through a STAGES-deep shared-memory ring filled by 1-D TMA bulk
-// copies (cp.async.bulk, one 9,216 B copy = the page's K and V blocks of this layer/head),
-// completion tracked by an mbarrier per stage; every wait is bounded.
+// Warp pair.  The Q.K^T warp streams each page's K block (4,608 B) and the P.V warp its V block
+// through their own 2-slot rings of 1-D bulk copies (cp.async.bulk), completion tracked by an
+// mbarrier per slot; P and the rescale factors pass from the first to the second through a
+// double-buffered shared-memory slot.  Every wait is bounded.
 //
-// Per page (64 tokens, the G <= 8 query heads of the group padded to n = 8):
-//   S^T = K^ . Q~^T on mma.sync m16n8k16 (fp16 in, fp32 accumulate): A = 2-bit K codes
-//     unpacked straight into fragments as fp16 (4 + c) with one shift + one LOP3 per pair,
-//     B = q (.) s_page (the per-channel K scales folded into the query, one HMUL2 per pair).
-//     k^ = s (2c - 3) = s (2 (4 + c) - 11), so the score is 2 raw - 11 sum(q~); sum(q~) comes
-//     from one more MMA chain with an all-ones A, so it uses exactly the rounded q~.
-//     The contraction order over the 256 dims is permuted so each thread's A and B come
-//     from 16 contiguous code bytes; any permutation of a dot product is the same sum.
-//   online softmax in FP32 (log2 domain), one max per page per head.
-//   O^T += V^ . P^T on the same MMA: A = V codes (4 + c) of two tokens per fp16 pair
-//     (byte permute + shift + LOP3), B = P (.) s_v (per-token V scale folded into P) moved
-//     from the S^T accumulator layout to the B layout with movmatrix.trans; the z offsets
-//     and the "+4" are added back with sum(P z) (FP32) and one all-ones MMA per k-step.
+// Per page (64 tokens, the G <= 8 query heads of the group padded to n = 8), on mma.sync
+// m16n8k16 (fp16 in, fp32 accumulate):
+//   S^T = K^ . Q~^T: A = the 2-bit K codes read straight as the fp16 numbers M + c (one LOP3 per
+//     register, see the A-operand notes below), B = q (.) s_page (the per-channel K scales
+//     folded into the query, one HMUL2 per pair); one more MMA chain with A = M + 1.5 gives
+//     sum q~ (M + 1.5), so q~ . k^ = 2 (sum q~ (M + c) - sum q~ (M + 1.5)) with exactly the
+//     rounded q~.  The per-token-K instance keeps q as B and applies each token's (s, z) to
+//     per-half sums instead.  The contraction order over the 256 dims is permuted so that each
+//     thread's A and B come from contiguous code bytes; a dot product does not depend on it.
+//   online softmax in FP32 (log2 domain) with a lazy rescale.
+//   O^T += V^ . P'^T: A = V codes of two tokens per fp16 pair (byte permute, LOP3, one HSUB2),
+//     B = P' = P (.) s_v (the per-token V scale folded into P, fp16) moved from the S^T
+//     accumulator layout to the B layout with movmatrix.trans; the zero points come back as
+//     sum P z in FP32.
 #include "kvq_internal.cuh"
 #include "attn_args.cuh"
 #include "append_ops.cuh"
