@@ -31,15 +31,16 @@ def _workload(lens, seed=2):
     return synth.Workload(f"pages_{lens}", 2, 2, 8, list(lens), t, total, window=64, seed=seed)
 
 
-@pytest.mark.parametrize("where", ["host", "device"])
-def test_gather_scatter_moves_pages_bit_exact(where):
+@pytest.mark.parametrize("where,fmt", [("host", oracle.FMT_HQ2B), ("device", oracle.FMT_HQ2B), ("device", oracle.FMT_FP8)])
+def test_gather_scatter_moves_pages_bit_exact(where, fmt):
+    """Pages of the 2-bit format and of the FP8 format move bit for bit."""
     from compressed_paged_kv_quant_gb300 import kvq
     from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
     wl = _workload([700, 130, 2000])
-    dw = DeviceWorkload(wl, kvq.FMT_HQ2B, "cuda", fill=0x5A)
+    dw = DeviceWorkload(wl, fmt, "cuda", fill=0x5A)
     dw.fill_history(wl.seq_len)
     torch.cuda.synchronize()
-    g = oracle.geom(oracle.FMT_HQ2B, wl.num_layers, wl.num_kv_heads, wl.num_q_heads)
+    g = oracle.geom(fmt, wl.num_layers, wl.num_kv_heads, wl.num_q_heads)
     pb = oracle.page_bytes(g)
     used = sorted({int(p) for p in wl.page_table.ravel() if p >= 0})
     ids = [used[i] for i in np.random.default_rng(4).permutation(len(used))]
@@ -59,7 +60,7 @@ def test_gather_scatter_moves_pages_bit_exact(where):
     # scatter into a second pool at other ids, repoint the page table, decode: same bits
     new_ids = [(p + 3) % wl.pool_pages for p in ids]
     remap = dict(zip(ids, new_ids))
-    dw2 = DeviceWorkload(wl, kvq.FMT_HQ2B, "cuda", fill=0x33)
+    dw2 = DeviceWorkload(wl, fmt, "cuda", fill=0x33)
     dw2.cache.ring.copy_(dw.cache.ring)               # the ring is per lane, not paged
     kvq.pages_scatter(dw2.g, dw2.cache.pool, torch.tensor(new_ids, dtype=torch.int32, device="cuda"), arena,
                       dw2.cache.status)

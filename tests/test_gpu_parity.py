@@ -325,20 +325,20 @@ def test_flat_attention_over_131072_keys_keeps_full_mass():
     assert_close(o, ref, atol=2e-4, rtol=2e-4, what="flat 131072")
 
 
-@pytest.mark.parametrize("window", [64, 32, 0])
-def test_decode_step_equals_append_then_decode(window):
-    """kvq_decode_step (the append inside the combine kernel, overlapped with the main kernel)
-    leaves the same pool and ring bytes as kv_quant_append followed by paged_decode_attn, and
-    the same outputs -- except, with window 0, lanes whose token closes a page, which are
-    checked against the oracle -- over 70 steps with page closes on every lane and
-    one lane that appends nothing on odd steps; windows 64, 32 and 0 put the closing page's keys
-    in the ring, split, and in the codes."""
+@pytest.mark.parametrize("fmt,window", [(HQ, 64), (HQ, 32), (HQ, 0), (TOK, 0), (HAD, 32), (FP8, 0)])
+def test_decode_step_equals_append_then_decode(fmt, window):
+    """kvq_decode_step (for the 2-bit format: the append, then the decode kernels overlapped with
+    it by programmatic dependent launch; for the other formats: the two calls in stream order)
+    leaves the same pool and ring bytes as kv_quant_append followed by paged_decode_attn and the
+    same outputs, bit for bit, over 70 steps with page closes on every lane and one lane that
+    appends nothing on odd steps; windows 64, 32 and 0 put the closing page's keys in the ring,
+    split, and in the codes."""
     from compressed_paged_kv_quant_gb300 import kvq
     steps = 70
     final = [700, 1500, 130, 3001]
     wl = _custom(final, L=2, H=2, Hq=12, seed=5, window=window)
     dev = "cuda"
-    A, B = _dw(wl, HQ), _dw(wl, HQ)
+    A, B = _dw(wl, fmt), _dw(wl, fmt)
     # lane 3 skips odd steps, so its history stops steps // 2 tokens short of its final length
     base = [n - steps for n in final[:3]] + [final[3] - steps // 2]
     for dw in (A, B):
