@@ -61,7 +61,8 @@ def test_gather_scatter_moves_pages_bit_exact(where, fmt):
     new_ids = [(p + 3) % wl.pool_pages for p in ids]
     remap = dict(zip(ids, new_ids))
     dw2 = DeviceWorkload(wl, fmt, "cuda", fill=0x33)
-    dw2.cache.ring.copy_(dw.cache.ring)               # the ring is per lane, not paged
+    if dw.cache.ring is not None:                      # the ring is per lane, not paged (FP8: none)
+        dw2.cache.ring.copy_(dw.cache.ring)
     kvq.pages_scatter(dw2.g, dw2.cache.pool, torch.tensor(new_ids, dtype=torch.int32, device="cuda"), arena,
                       dw2.cache.status)
     pt2 = np.vectorize(lambda p: remap.get(int(p), -1) if p >= 0 else -1)(wl.page_table).astype(np.int32)

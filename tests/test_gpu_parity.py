@@ -374,4 +374,5 @@ def test_decode_step_equals_append_then_decode(fmt, window):
         pos = seq
     assert pos == final
     assert torch.equal(A.cache.pool, B.cache.pool)
-    assert torch.equal(A.cache.ring, B.cache.ring)
+    assert (A.cache.ring is None) == (B.cache.ring is None)              # the FP8 format has no ring
+    assert A.cache.ring is None or torch.equal(A.cache.ring, B.cache.ring)
