@@ -81,6 +81,22 @@ def _decode_traffic():
     return None
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x: a job of N replicas takes as long as its slowest rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, ms: float) -> float:
+    """Whole-job tokens per second: every rank processes tokens_per_step per step (weak scaling)."""
+    return world * tokens_per_step / (ms / 1000.0)
+
+
 def _config(extra=None, fmt="hq2b"):
     pages = "FP8 E4M3 pages (256 B/head/token each for K and V)" if fmt == "fp8" else "2-bit pages (72 B/head/token)"
     c = {"workload": "decode_27b_8x40960: 16 layers x 4 KV heads x 256, 24 q heads, 8 lanes x 40,960 tokens, "
@@ -306,13 +322,10 @@ def run_gpu(args):
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     assert dw.cache.read_status() == 0, "device status flagged during the timed steps"
     tokens_per_step = lanes * ctx
-    value = world * tokens_per_step / (ms / 1000.0)
+    value = job_throughput(world, tokens_per_step, ms)
 
     # per-call duration of the attention: the L decode calls of one step captured alone in a
     # graph (no host launch gaps), CUDA events on the launching stream around its replays
@@ -357,12 +370,8 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * tokens_per_step / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    e2e_value = job_throughput(world, tokens_per_step, e2e_ms)
 
     moves = None if args.no_page_moves else run_page_moves(dw, stream)
     prefill = None if (args.no_prefill or args.format != "hq2b") else run_prefill(args, dev, stream)
