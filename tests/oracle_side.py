@@ -11,6 +11,7 @@ import oracle
 from compressed_paged_kv_quant_gb300 import synth
 
 ATOL, RTOL = 2e-3, 1e-3          # |gpu - oracle| <= ATOL + RTOL * |oracle|, elementwise
+TWO_BIT = (oracle.FMT_HQ2B, oracle.FMT_HQ2B_HAD, oracle.FMT_HQ2B_TOK)   # formats with the exact-key ring
 THREADS = max(1, min(32, os.cpu_count() or 1))
 
 
@@ -45,7 +46,7 @@ class LaneCache:
         npg = (n + 63) // 64
         self.pt = np.arange(npg, dtype=np.int32)[None, :]
         self.pool = np.full(max(npg, 1) * self.pb, fill, np.uint8)
-        self.ring = np.zeros((1, 1, wl.num_kv_heads, 64, 256), np.uint16) if fmt == oracle.FMT_HQ2B else None
+        self.ring = np.zeros((1, 1, wl.num_kv_heads, 64, 256), np.uint16) if fmt in TWO_BIT else None
         self.k = host_kv(wl, layer, lane, 0, n, 0)
         self.v = host_kv(wl, layer, lane, 0, n, 1)
         st = oracle.append(self.g, 0, self.pool, self.ring, self.pt, 1, [0], [n], [0], self.k, self.v)
@@ -78,6 +79,6 @@ class LaneCache:
 def gpu_block(pool_u8: np.ndarray, page_bytes: int, num_kv_heads: int, fmt: int, phys: int, layer: int,
               head: int, kv: int) -> np.ndarray:
     """Bytes of one (layer, head, K/V) block of physical page `phys` of a copied-back pool."""
-    bb = 4608 if fmt == oracle.FMT_HQ2B else 32768
+    bb = 64 * oracle.head_token_bytes(fmt)
     off = phys * page_bytes + ((layer * num_kv_heads + head) * 2 + kv) * bb
     return pool_u8[off:off + bb]

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from compressed_paged_kv_quant_gb300 import synth
-from oracle_side import LaneCache, assert_close, gpu_block
+from oracle_side import TWO_BIT, LaneCache, assert_close, gpu_block
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
@@ -62,7 +62,7 @@ def _check_lane(dw, wl, fmt, layer, lane, got, pages=(0, 1)):
             for kv in (0, 1):
                 g_blk = gpu_block(blk, pb, wl.num_kv_heads, fmt, 0, layer, h, kv)
                 np.testing.assert_array_equal(g_blk, oc.block(p, h, kv), err_msg=f"page {p} head {h} kv {kv}")
-    if fmt == HQ:
+    if fmt in TWO_BIT:
         ring = _u16(dw.cache.ring).reshape(wl.lanes, wl.num_layers, wl.num_kv_heads, 64, 256)
         np.testing.assert_array_equal(ring[lane, layer], oc.ring[0, 0])
     return err, oc
@@ -80,6 +80,20 @@ def test_batched_decode_27b_sampled():
         _check_lane(dw, wl, HQ, layer, lane, outs[layer][lane])
     for l in range(wl.num_layers):
         assert np.all(np.isfinite(outs[l]))
+
+
+@pytest.mark.parametrize("fmt", [oracle.FMT_HQ2B_HAD, oracle.FMT_HQ2B_TOK, oracle.FMT_FP8])
+def test_batched_decode_27b_format_variants_sampled(fmt):
+    """The 27B decode workload's per-layer sizes (8 lanes x 40,960 tokens, 4 KV heads, 24 q
+    heads; two layers) in the rotated, per-token-K and FP8 formats, through the step the
+    benchmark times for them (append, then decode); two (layer, lane) pairs compared in full."""
+    wl = synth.batched_decode_27b(layers=2)
+    dw = _dw(wl, fmt, fill=None)
+    dw.fill_history([n - 1 for n in wl.seq_len])
+    outs = _decode_step(dw, range(wl.num_layers))
+    assert dw.cache.read_status() == 0
+    for layer, lane in ((0, 3), (1, 7)):
+        _check_lane(dw, wl, fmt, layer, lane, outs[layer][lane])
 
 
 def test_mixed_shared_prefix_window64_sampled():
