@@ -13,7 +13,8 @@
 //   2. rows:   one warp per (token, head) quantizes the V row, and stores the K row in the
 //      ring (only the chunk's last 64 tokens -- the ring keeps the newest key of each slot).
 // Launch 1 must read the ring before launch 2 overwrites it; stream order guarantees that.
-// Decode steps (max_new == 1): one launch does both for each (lane, head).
+// Decode steps (max_new == 1): one launch does both for each (lane, head), the page close split
+// over four CTAs of 64 channels each.
 // The per-token-K format (KVQ_FMT_HQ2B_TOK) codes the K row with the V rule in the rows pass and
 // has no page close.
 // All quantizer arithmetic is IEEE fp32 round-to-nearest-even (__fdiv_rn, __fsub_rn, ...,
@@ -46,20 +47,25 @@ __global__ void __launch_bounds__(256) append_rows_kernel(AppendArgs a) {
   }
 }
 
-// Decode-time append (at most one new token per lane) in one launch: CTA (lane b, head h); warp
-// 0 writes the token's row, and when the token closes its page every thread quantizes the
-// page's K block.  The page close reads ring slots 0..62 and this token's key from `k`; the row
-// write touches slot 63 only, so the two never meet.
-template <int FMT>
-__global__ void __launch_bounds__(KCLOSE_THREADS) append_one_kernel(AppendArgs a) {
+// Decode-time append (at most one new token per lane) in one launch: CTA (lane b, head h,
+// channel group z); warp 0 of group 0 writes the token's row, and when the token closes its
+// page, each group's CTA quantizes its KGROUP_CH channels of the page's K block (THREADS =
+// KGROUP_THREADS, 4 groups), or one 1,024-thread CTA the whole block (the rotated format, whose
+// keys are rotated a row at a time).  The page close reads ring slots 0..62 and this token's key
+// from `k`; the row write touches slot 63 only, so the two never meet.
+template <int FMT, int THREADS>
+__global__ void __launch_bounds__(THREADS) append_one_kernel(AppendArgs a) {
   // a decode kernel launched as this grid's programmatic dependent (kvq_decode_step) may start
   // now; it waits for this grid before it reads anything written here
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  const int b = blockIdx.x, h = blockIdx.y;
+  const int b = blockIdx.x, h = blockIdx.y, grp = blockIdx.z;
   int start, n, off;
   if (!read_lane(a, b, start, n, off) || n == 0) return;
-  if (threadIdx.x < 32) append_row<FMT>(a, b, h, 0, start, n, off);
-  if (FMT == KVQ_FMT_HQ2B && !a.c.ktok && (start + 1) % P == 0) kclose_page(a, b, h, start / P, start, off);
+  if (grp == 0 && threadIdx.x < 32) append_row<FMT>(a, b, h, 0, start, n, off);
+  if (FMT == KVQ_FMT_HQ2B && !a.c.ktok && (start + 1) % P == 0) {
+    if constexpr (THREADS == KCLOSE_THREADS) kclose_page(a, b, h, start / P, start, off);
+    else kclose_group(a, b, h, start / P, start, off, grp);
+  }
 }
 
 int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* ring, const int32_t* start_pos,
@@ -68,9 +74,16 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
   AppendArgs a{c, pool, ring, start_pos, n_new, tok_offset, max_new, n_rows, lanes, k, v};
   if (max_new == 1) {
     dim3 g1(lanes, c.num_kv_heads);
-    if (fmt == KVQ_FMT_HQ2B) append_one_kernel<KVQ_FMT_HQ2B><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
-    else if (fmt == KVQ_FMT_FP8) append_one_kernel<KVQ_FMT_FP8><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
-    else append_one_kernel<KVQ_FMT_BF16><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
+    if (fmt == KVQ_FMT_HQ2B && c.rotated) {
+      append_one_kernel<KVQ_FMT_HQ2B, KCLOSE_THREADS><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
+    } else if (fmt == KVQ_FMT_HQ2B) {
+      const dim3 gg(lanes, c.num_kv_heads, c.ktok ? 1 : D / KGROUP_CH);
+      append_one_kernel<KVQ_FMT_HQ2B, KGROUP_THREADS><<<gg, KGROUP_THREADS, 0, stream>>>(a);
+    } else if (fmt == KVQ_FMT_FP8) {
+      append_one_kernel<KVQ_FMT_FP8, KGROUP_THREADS><<<g1, KGROUP_THREADS, 0, stream>>>(a);
+    } else {
+      append_one_kernel<KVQ_FMT_BF16, KGROUP_THREADS><<<g1, KGROUP_THREADS, 0, stream>>>(a);
+    }
   } else if (fmt == KVQ_FMT_HQ2B) {
     if (!c.ktok) {   // the per-token-K format has no page close
       dim3 gk(max_new / P + 1, c.num_kv_heads, lanes);
