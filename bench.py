@@ -30,9 +30,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 # page formats by name: the binding's (and the oracle's) format constant
-FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD", "hq2b_tok": "FMT_HQ2B_TOK", "fp8": "FMT_FP8"}
+FORMATS = {"hq2b": "FMT_HQ2B", "hq2b_had": "FMT_HQ2B_HAD", "hq2b_tok": "FMT_HQ2B_TOK", "fp8": "FMT_FP8",
+           "bf16": "FMT_BF16"}
 # bytes one head's one token costs for K plus V in each format
-KV_BYTES = {"hq2b": 144, "hq2b_had": 144, "hq2b_tok": 144, "fp8": 512}
+KV_BYTES = {"hq2b": 144, "hq2b_had": 144, "hq2b_tok": 144, "fp8": 512, "bf16": 1024}
 WORKLOAD = dict(lanes=8, ctx=40960, layers=16, kv_heads=4, q_heads=24)
 METRIC = "decode attn: compressed-KV tokens/s & achieved HBM GB/s (% of peak); prefill TFLOP/s"
 UNIT = "tokens/s"
@@ -98,7 +99,8 @@ def job_throughput(world: int, tokens_per_step: int, ms: float) -> float:
 
 
 def _config(extra=None, fmt="hq2b"):
-    pages = "FP8 E4M3 pages (256 B/head/token each for K and V)" if fmt == "fp8" else "2-bit pages (72 B/head/token)"
+    pages = {"fp8": "FP8 E4M3 pages (256 B/head/token each for K and V)",
+             "bf16": "BF16 pages (512 B/head/token each for K and V)"}.get(fmt, "2-bit pages (72 B/head/token)")
     c = {"workload": "decode_27b_8x40960: 16 layers x 4 KV heads x 256, 24 q heads, 8 lanes x 40,960 tokens, "
                      f"{pages}, append + decode per layer",
          "lanes": WORKLOAD["lanes"], "context_tokens": WORKLOAD["ctx"], "layers": WORKLOAD["layers"],
@@ -399,7 +401,9 @@ def run_gpu(args):
                                          "decode_hq2b_combine), one layer") if args.format == "hq2b_had" else
                                         ("paged_decode_attn (decode_hq2b_main<per-token K> + decode_hq2b_combine), "
                                          "one layer") if args.format == "hq2b_tok" else
-                                        "paged_decode_attn (decode_fp8_split + attn_combine), one layer"),
+                                        "paged_decode_attn (decode_fp8_split + attn_combine), one layer"
+                                        if args.format == "fp8" else
+                                        "paged_decode_attn (attn_split_generic + attn_combine, CUDA cores), one layer"),
                              "algorithmic_bytes_per_launch": attn_bytes},
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -544,7 +548,8 @@ def main():
     ap.add_argument("--layers", type=int, default=WORKLOAD["layers"])
     ap.add_argument("--format", default="hq2b", choices=sorted(FORMATS),
                     help="page format: hq2b (the benchmark's), hq2b_had (Walsh-Hadamard-rotated 2-bit), "
-                         "hq2b_tok (K per token) or fp8 (E4M3); the variants time decode only")
+                         "hq2b_tok (K per token), fp8 (E4M3) or bf16 (the exact reference path); the "
+                         "variants time decode only")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-page-moves", action="store_true")
     ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],
