@@ -154,3 +154,24 @@ def test_prefill_host_validation(L):
 def test_strerror(L):
     for code in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(kvq.strerror(code), str) and kvq.strerror(code)
+
+
+def test_format_variants_host_validation(L):
+    """Host-side answers for the format variants, all returned before any launch: the 2-bit
+    variants need the ring, FP8 does not; a bad FP8 scale is refused by every call; the rotated
+    format refuses prefill."""
+    tok = kvq.geom(kvq.FMT_HQ2B_TOK, 2, 1, 4)
+    had = kvq.geom(kvq.FMT_HQ2B_HAD, 2, 1, 4)
+    assert _decode(L, tok, ring=None) == kvq.ERR_INVALID_ARG
+    assert _decode(L, had, ring=None) == kvq.ERR_INVALID_ARG
+    assert _decode(L, tok, ws_bytes=64) == kvq.ERR_WORKSPACE_TOO_SMALL
+    fp8 = kvq.geom(kvq.FMT_FP8, 2, 1, 4)
+    assert _decode(L, fp8, ring=None, ws_bytes=64) == kvq.ERR_WORKSPACE_TOO_SMALL   # no ring needed
+    assert _decode(L, fp8, ring=None, lanes=0) == kvq.OK
+    bad = kvq.geom(kvq.FMT_FP8, 2, 1, 4, k_scale=-2.0)
+    assert _decode(L, bad, ring=None) == kvq.ERR_INVALID_ARG
+    assert L.kv_quant_append(ctypes.byref(bad), 0, 256, 1 << 24, None, 768, 4, 1, 1024, 1040, 1056, 1, 1,
+                             1280, 1536, 2048, None) == kvq.ERR_INVALID_ARG
+    rc = L.paged_prefill_attn(ctypes.byref(had), 0, 256, 1 << 22, 512, 0, 768, 4, 1, 1024, 1040, 1056, 16, 16,
+                              1072, 256, 1280, 0.0625, 1536, 1 << 24, 1792, 2048, None)
+    assert rc == kvq.ERR_UNSUPPORTED
