@@ -118,6 +118,17 @@ def v_rule(x: np.ndarray, axis: int = 1) -> np.ndarray:
     return z + c * s
 
 
+def rotated(rule):
+    """`rule` applied to rows turned by the orthonormal Sylvester Hadamard matrix of the row
+    length (H = H^T = H^-1), the result turned back: the rotated variant's order of steps."""
+    from scipy.linalg import hadamard
+
+    def q(x):
+        h = hadamard(x.shape[1]).astype(np.float64) / np.sqrt(x.shape[1])
+        return rule(x @ h) @ h
+    return q
+
+
 def four_level_tables(trials: int = TRIALS):
     """(reconstruction rows, needle rows) on this format's 2-bit grids, same synthetic caches."""
     rng = np.random.default_rng(SEED)
@@ -129,9 +140,12 @@ def four_level_tables(trials: int = TRIALS):
         ("K", "per-token (V rule, 128 dims)", _rel(v_rule(k, 1), k)),
         ("V", "per-token (V rule, 128 dims)", _rel(v_rule(v, 1), v)),
         ("V", "per-channel (V rule, 64-token page)", _rel(v_rule(v, 0), v)),
+        ("K", "per-channel after a Hadamard rotation", _rel(rotated(k_rule_per_channel)(k), k)),
+        ("K", "per-token after a Hadamard rotation", _rel(rotated(v_rule)(k), k)),
     ]
     needle = []
-    for name, kq in (("K per-channel (K rule)", k_rule_per_channel), ("K per-token (V rule)", v_rule)):
+    for name, kq in (("K per-channel (K rule)", k_rule_per_channel), ("K per-token (V rule)", v_rule),
+                     ("K per-channel, rotated", rotated(k_rule_per_channel)), ("K per-token, rotated", rotated(v_rule))):
         f, we, oe = _needle_trials(np.random.default_rng(SEED + 1), kq, v_rule, trials)
         needle.append((name, f, trials, we, oe))
     return recon, needle
