@@ -93,10 +93,15 @@ CacheView make_view(const kvq_geom* g, int layer, const void* pool, size_t pool_
   return c;
 }
 
-// Checks shared by the attention entry points.
+}  // namespace
+
+namespace kvq {
+// Checks shared by the attention entry points (the workspace pointer too unless
+// need_workspace is false: the no-allocation decode supplies its own).
 int check_attn_common(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
                       int window, const int32_t* page_table, int max_pages, int lanes, const int32_t* seq_len,
-                      int max_seq_len, const void* q, void* workspace, float* out, int32_t* d_status) {
+                      int max_seq_len, const void* q, void* workspace, float* out, int32_t* d_status,
+                      bool need_workspace) {
   int rc = check_geom(g);
   if (rc) return rc;
   if (layer < 0 || layer >= g->num_layers || lanes < 0 || max_pages < 0 || max_seq_len < 0) return KVQ_ERR_INVALID_ARG;
@@ -104,13 +109,17 @@ int check_attn_common(const kvq_geom* g, int layer, const void* pool, size_t poo
   if ((int64_t)max_seq_len > (int64_t)max_pages * P) return KVQ_ERR_INVALID_ARG;
   if ((int64_t)max_pages * P > (int64_t)INT32_MAX) return KVQ_ERR_INVALID_ARG;
   if (lanes == 0) return KVQ_OK;
-  if (!pool || !page_table || !seq_len || !q || !workspace || !out || !d_status) return KVQ_ERR_INVALID_ARG;
+  if (!pool || !page_table || !seq_len || !q || (need_workspace && !workspace) || !out || !d_status)
+    return KVQ_ERR_INVALID_ARG;
   if (two_bit(g->format) && !ring) return KVQ_ERR_INVALID_ARG;
   if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(pool) || !aligned16(ring) || !aligned16(q) || !aligned16(workspace) || !aligned16(out))
     return KVQ_ERR_ALIGNMENT;
   return KVQ_OK;
 }
+}  // namespace kvq
+
+namespace {
 
 AttnArgs decode_args(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring, int window,
                      const int32_t* page_table, int max_pages, int lanes, const int32_t* seq_len, int max_seq_len,
@@ -206,7 +215,7 @@ int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t poo
                       int max_seq_len, const void* q, float sm_scale, void* workspace, size_t ws_bytes,
                       float* out, int32_t* d_status, kvq_stream_t stream) {
   int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
-                             max_seq_len, q, workspace, out, d_status);
+                             max_seq_len, q, workspace, out, d_status, true);
   if (rc || lanes == 0) return rc;
   if (ws_bytes < kvq_decode_workspace_bytes(g, lanes, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
   AttnArgs a = decode_args(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
@@ -228,7 +237,7 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
                        const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale, void* workspace,
                        size_t ws_bytes, float* out, int32_t* d_status, kvq_stream_t stream) {
   int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
-                             max_seq_len, q, workspace, out, d_status);
+                             max_seq_len, q, workspace, out, d_status, true);
   if (rc) return rc;
   if (g->format == KVQ_FMT_HQ2B_HAD) return KVQ_ERR_UNSUPPORTED;   // no rotated prefill kernel
   if (max_n_q < 0 || n_q_rows < 0) return KVQ_ERR_INVALID_ARG;
@@ -269,7 +278,7 @@ int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes,
                     const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale, void* workspace,
                     size_t ws_bytes, float* out, int32_t* d_status, kvq_stream_t stream) {
   int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
-                             max_seq_len, q, workspace, out, d_status);
+                             max_seq_len, q, workspace, out, d_status, true);
   if (rc) return rc;
   if (n_rows < 0) return KVQ_ERR_INVALID_ARG;
   if (lanes == 0) return KVQ_OK;

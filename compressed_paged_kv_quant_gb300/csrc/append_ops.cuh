@@ -286,6 +286,13 @@ __device__ __forceinline__ void kclose_group(const AppendArgs& a, int b, int h, 
     amax = fmaxf(amax, fabsf(x[i]));
   }
   part_max[part][cl] = amax;
+  // every channel of the page's keys that come from this call's input rows (ring rows were
+  // checked when they were appended): a bad value anywhere in them leaves the whole K block
+  // unwritten, in all four group CTAs alike, as a whole-page close would
+  for (int i = threadIdx.x, first = max(0, start - p * P); i < (P - first) * D; i += KGROUP_THREADS) {
+    const int pos = p * P + first + i / D;
+    bad |= !finite16(__bfloat162float(a.k[((int64_t)(off + pos - start) * H + h) * D + i % D]));
+  }
   if (__syncthreads_or(bad)) {
     if (threadIdx.x == 0) flag(c.status, KVQ_STATUS_BAD_INPUT);
     return;

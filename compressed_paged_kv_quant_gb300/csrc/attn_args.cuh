@@ -35,14 +35,25 @@ struct AttnArgs {
   __half* q_rot;     // rotated format: H q per (lane, query head) in fp16 (workspace), else null
 };
 
+// Status bits for a lane length no kernel may use (0 when it is usable): past the page table
+// (LEN_GT_TABLE), or negative or above the host bound max_seq_len that sized the grid and the
+// split records of the workspace (BAD_LEN).  A lane that fails is skipped by every kernel of the
+// call, so no kernel indexes a split record beyond the lane's share of the workspace.
+__device__ __forceinline__ int lane_len_error(const AttnArgs& a, int len) {
+  if (len < 0) return KVQ_STATUS_BAD_LEN;
+  if (len > a.c.max_pages * P) return KVQ_STATUS_LEN_GT_TABLE;
+  if (len > a.max_seq_len) return KVQ_STATUS_BAD_LEN;
+  return 0;
+}
+
 // Resolve query i of lane b: its row, position, and key count.  Returns false (after
 // flagging) when the lane's arguments are invalid or i is past the lane's queries.
 __device__ __forceinline__ bool resolve_query(const AttnArgs& a, bool decode, int b, int i, int& row, int& n_keys,
                                               int& len, bool flag_errors) {
   const CacheView& c = a.c;
   len = a.seq_len[b];
-  if (len < 0 || len > c.max_pages * P) {
-    if (flag_errors) flag(c.status, len < 0 ? KVQ_STATUS_BAD_LEN : KVQ_STATUS_LEN_GT_TABLE);
+  if (const int e = lane_len_error(a, len)) {
+    if (flag_errors) flag(c.status, e);
     return false;
   }
   if (decode) {

@@ -69,8 +69,8 @@ __global__ void __launch_bounds__(F8_WARPS * 32, F8_CTAS) decode_fp8_split(AttnA
   const int b = blockIdx.x / H, h = blockIdx.x % H, s = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, cq = lane & 3;
   const int len = a.seq_len[b];
-  if (len < 0 || len > c.max_pages * P) {
-    if (threadIdx.x == 0 && s == 0 && h == 0) flag(c.status, KVQ_STATUS_LEN_GT_TABLE);
+  if (const int e = lane_len_error(a, len)) {
+    if (threadIdx.x == 0 && s == 0 && h == 0) flag(c.status, e);
     return;
   }
   const int t0 = s * a.split_tokens;

@@ -49,14 +49,15 @@ constexpr int DEC_CTAS_PER_SM = KVQ_DEC_CTAS_PER_SM;  // resident CTAs per SM th
 constexpr int MIN_PAGES_PER_WARP = 2;
 constexpr int DEC_MAX_SLOTS = 96;            // partial records per (lane, query head), at most
 
-// pages of lane b handled by the MMA path (everything before its exact tail)
-__device__ __forceinline__ int main_pages(const CacheView& c, const int32_t* seq_len, int b, bool* bad = nullptr) {
-  const int len = seq_len[b];
-  if (len < 0 || len > c.max_pages * P) {
-    if (bad) *bad = true;
+// pages of lane b handled by the MMA path (everything before its exact tail); a lane whose
+// length is unusable has none, and *err (if given) receives its status bits
+__device__ __forceinline__ int main_pages(const AttnArgs& a, int b, int* err = nullptr) {
+  const int len = a.seq_len[b];
+  if (const int e = lane_len_error(a, len)) {
+    if (err) *err = e;
     return 0;
   }
-  const int ef = exact_from(len, c.window, c.ktok);
+  const int ef = exact_from(len, a.c.window, a.c.ktok);
   return ef <= 0 ? 0 : ef / P;
 }
 
@@ -204,9 +205,9 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
     int carry = 0;
     for (int base = 0; base < a.lanes; base += 32) {
       const int b = base + lane;
-      bool bad = false;
-      int n = b < a.lanes ? main_pages(c, a.seq_len, b, &bad) : 0;
-      if (bad && blockIdx.x == 0) flag(c.status, KVQ_STATUS_LEN_GT_TABLE);
+      int err = 0;
+      int n = b < a.lanes ? main_pages(a, b, &err) : 0;
+      if (err && blockIdx.x == 0) flag(c.status, err);
       int incl = n;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -677,7 +678,7 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
   // main pages of lanes before b, and of all lanes
   int before = 0, total = 0;
   for (int i = tid; i < a.lanes; i += blockDim.x) {
-    const int n = main_pages(c, a.seq_len, i);
+    const int n = main_pages(a, i);
     total += n;
     if (i < b) before += n;
   }
@@ -691,8 +692,8 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
     s_sum[1][warp] = total;
   }
   const int len = a.seq_len[b];
-  const bool bad = len < 0 || len > c.max_pages * P;
-  const int npg = bad ? 0 : main_pages(c, a.seq_len, b);
+  const bool bad = lane_len_error(a, len) != 0;
+  const int npg = bad ? 0 : main_pages(a, b);
   const int ef = bad ? 0 : exact_from(len, c.window, c.ktok);
   const int tail_start = npg * P;
   const int ntail = bad ? 0 : len - tail_start;

@@ -1,11 +1,16 @@
 // decode_noalloc.cu -- paged_decode_attn for callers that cannot allocate device memory.
 //
-// Some callers cannot call cudaMalloc at all: code that runs inside a captured CUDA graph
-// region it does not own, plugins of an engine whose allocator owns every byte of the GPU,
-// or hosts whose memory budget forbids any allocation after start-up.  They still need the
-// split-K decode, which keeps its per-split partials (m, l, acc[256] in FP32) in scratch
-// memory.  This entry point takes that scratch from one file-scope device array of a fixed
-// size instead of a caller-provided workspace; the caller still passes inputs and outputs.
+// Some callers cannot call cudaMalloc at all: plugins of a serving engine whose allocator owns
+// every byte of the GPU and hands out no scratch, hosts whose memory budget forbids any
+// allocation after start-up, and latency-critical loops where an allocation (which may
+// synchronise the device) is not allowed.  They still need the split-K decode, which keeps its
+// per-split partials (m, l, acc[256] in FP32) in scratch memory.  This entry point takes that
+// scratch from one file-scope device array of a fixed size instead of a caller-provided
+// workspace; the caller still passes inputs and outputs.
+//
+// Set-up: the first call on a device looks up the array's device address with
+// cudaGetSymbolAddress, once per device, with that device current; make that first call before
+// any stream capture begins.
 //
 // The array lives in every GPU that loads the library, for as long as the process runs.
 // Every call shares it: two calls whose kernels overlap on the GPU (different streams, no
@@ -15,6 +20,13 @@
 #include <mutex>
 
 #include "kvq_internal.cuh"
+
+namespace kvq {
+int check_attn_common(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
+                      int window, const int32_t* page_table, int max_pages, int lanes, const int32_t* seq_len,
+                      int max_seq_len, const void* q, void* workspace, float* out, int32_t* d_status,
+                      bool need_workspace);
+}  // namespace kvq
 
 namespace {
 
@@ -49,9 +61,11 @@ int paged_decode_attn_noalloc(const kvq_geom* geom, int layer, const void* pool,
                               const void* ring, int window, const int32_t* page_table, int max_pages, int lanes,
                               const int32_t* seq_len, int max_seq_len, const void* q, float sm_scale, float* out,
                               int32_t* d_status, kvq_stream_t stream) {
-  const size_t need = kvq_decode_workspace_bytes(geom, lanes, max_seq_len);
-  if (need == 0 && lanes > 0) return kvq_page_bytes(geom) == 0 ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_INVALID_ARG;
-  if (need > SCRATCH_BYTES) return KVQ_ERR_SCRATCH_LIMIT;
+  // the arguments are checked exactly as paged_decode_attn checks them, before the limit
+  const int crc = kvq::check_attn_common(geom, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes,
+                                         seq_len, max_seq_len, q, nullptr, out, d_status, false);
+  if (crc || lanes == 0) return crc;
+  if (kvq_decode_workspace_bytes(geom, lanes, max_seq_len) > SCRATCH_BYTES) return KVQ_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc) return rc;

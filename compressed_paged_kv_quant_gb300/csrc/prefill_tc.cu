@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
   // ---- rows and keys of this CTA (uniform: early exits happen before any barrier)
   const int len = a.seq_len[b];
   const int nq = a.n_q[b], qoff = a.q_offset[b], qpos0 = a.q_pos0[b];
-  if (len < 0 || len > c.max_pages * P || nq < 0 || nq > a.max_n_q || qoff < 0 || (int64_t)qoff + nq > a.n_q_rows ||
+  if (lane_len_error(a, len) || nq < 0 || nq > a.max_n_q || qoff < 0 || (int64_t)qoff + nq > a.n_q_rows ||
       qpos0 < 0 || (int64_t)qpos0 + nq > len) {
     if (threadIdx.x == 0 && s == 0 && qt == 0 && h == 0) flag(c.status, KVQ_STATUS_BAD_LEN);
     return;

@@ -94,7 +94,8 @@ typedef struct {
 #define KVQ_STATUS_PAGE_OOB 1      /* a page-table entry the call needed is outside [0, pool pages) */
 #define KVQ_STATUS_LEN_GT_TABLE 2  /* a position lies past max_pages * 64 */
 #define KVQ_STATUS_BAD_INPUT 4     /* a K/V input is NaN, Inf or |x| > 65504 (not quantized) */
-#define KVQ_STATUS_BAD_LEN 8       /* a negative count, n_new > max_new, rows past n_rows, or a
+#define KVQ_STATUS_BAD_LEN 8       /* a negative count, n_new > max_new, rows past n_rows, a
+                                      seq_len[b] above max_seq_len (that lane is skipped), or a
                                       prefill query position >= seq_len */
 #define KVQ_STATUS_TIMEOUT 16      /* a bounded wait on a shared-memory barrier gave up */
 
@@ -249,15 +250,17 @@ int kvq_pages_scatter(const kvq_geom* geom, void* pool, size_t pool_bytes, const
 /*
  * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.  The pages have
  * no counterpart of this call: it exists for callers that cannot allocate device memory --
- * code running inside a CUDA graph capture it does not own, plugins of an engine whose
- * allocator owns all of the GPU's memory, hosts that forbid allocation after start-up.
+ * plugins of a serving engine whose allocator owns all of the GPU's memory and hands out no
+ * scratch, hosts that forbid allocation after start-up, latency-critical loops where an
+ * allocation (which may synchronise the device) is not allowed.
  *   Same arguments, results and errors as paged_decode_attn, minus `workspace`/`ws_bytes`:
  *   the split partials live in one static device array of KVQ_NOALLOC_SCRATCH_BYTES
  *   (32 MiB) inside the library, which every GPU that loads the library keeps until the
  *   process exits.  The call allocates nothing and calls no allocating routine.
  *   Limit: kvq_decode_workspace_bytes(geom, lanes, max_seq_len) must not exceed
  *   KVQ_NOALLOC_SCRATCH_BYTES, else KVQ_ERR_SCRATCH_LIMIT and nothing is launched (at the
- *   27B geometry that is room for 8 lanes x 40,960 tokens several times over).
+ *   27B geometry that is room for 8 lanes x 40,960 tokens several times over).  Every other
+ *   argument is checked first, with the codes paged_decode_attn returns.
  *   The first call on a device looks up the array's device address (once per device, with
  *   that device current); make that first call before any stream capture.
  *   Every call shares the array: calls whose kernels may overlap on the GPU (different

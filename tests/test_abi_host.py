@@ -175,3 +175,33 @@ def test_format_variants_host_validation(L):
     rc = L.paged_prefill_attn(ctypes.byref(had), 0, 256, 1 << 22, 512, 0, 768, 4, 1, 1024, 1040, 1056, 16, 16,
                               1072, 256, 1280, 0.0625, 1536, 1 << 24, 1792, 2048, None)
     assert rc == kvq.ERR_UNSUPPORTED
+
+
+def _noalloc(L, g, **kw):
+    a = dict(layer=0, pool=256, pool_bytes=1 << 24, ring=512, window=0, pt=768, max_pages=4, lanes=1,
+             seq_len=1024, max_seq_len=256, q=1280, scale=0.0625, out=1792, status=2048)
+    a.update(kw)
+    gp = ctypes.byref(g) if g is not None else None
+    return L.paged_decode_attn_noalloc(gp, a["layer"], a["pool"], a["pool_bytes"], a["ring"], a["window"], a["pt"],
+                                       a["max_pages"], a["lanes"], a["seq_len"], a["max_seq_len"], a["q"],
+                                       a["scale"], a["out"], a["status"], None)
+
+
+def test_noalloc_host_validation_matches_decode(L):
+    """The no-allocation decode checks its arguments exactly as paged_decode_attn does, before
+    its own scratch limit, and refuses a request over the limit before anything is launched."""
+    g = kvq.geom(kvq.FMT_HQ2B, 2, 1, 4)
+    assert L.paged_decode_attn_noalloc(None, 0, 256, 1 << 24, 512, 0, 768, 4, 1, 1024, 256, 1280, 0.0625, 1792,
+                                       2048, None) == kvq.ERR_INVALID_ARG
+    bad_group = kvq.geom(kvq.FMT_HQ2B, 2, 4, 10)          # 10 query heads over 4 KV heads
+    assert _noalloc(L, bad_group) == _decode(L, bad_group) == kvq.ERR_INVALID_ARG
+    wide_group = kvq.geom(kvq.FMT_HQ2B, 2, 1, 12)          # group 12 > 8
+    assert _noalloc(L, wide_group) == _decode(L, wide_group) == kvq.ERR_UNSUPPORTED
+    for kw in (dict(layer=2), dict(window=65), dict(max_seq_len=257), dict(ring=None), dict(q=None),
+               dict(pool_bytes=100), dict(q=1288), dict(out=None), dict(status=None)):
+        assert _noalloc(L, g, **kw) == _decode(L, g, **kw), kw
+    assert _noalloc(L, g, lanes=0) == kvq.OK
+    # 4,096 lanes of 2^22 tokens need far more than the static scratch: refused on the host
+    huge = 1 << 22
+    assert kvq.decode_workspace_bytes(g, 4096, huge) > kvq.NOALLOC_SCRATCH_BYTES
+    assert _noalloc(L, g, lanes=4096, max_seq_len=huge, max_pages=huge // 64) == kvq.ERR_SCRATCH_LIMIT

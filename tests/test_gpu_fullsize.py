@@ -31,18 +31,38 @@ def _u16(t):
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def _decode_step(dw, layers):
-    """The benchmark's step: append each lane's token, then decode, per layer."""
+def _decode_step(dw, layers, fused=True):
+    """One decode step over `layers`.  fused=True is the benchmark's launch configuration: every
+    layer's kvq_decode_step (append + decode kernels overlapped by programmatic dependent
+    launch) back to back, captured once in a CUDA graph and replayed, with one workspace shared
+    by the layers and one output buffer per layer.  fused=False: kv_quant_append then
+    paged_decode_attn, eagerly, with a garbage-filled workspace before each layer."""
+    layers = list(layers)
     ws, out = dw.decode_buffers()
-    outs = {}
+    ws.view(torch.int32).fill_(-1)
+    outs = torch.empty((len(layers),) + tuple(out.shape), dtype=out.dtype, device=out.device)
+    qkv = []
     for l in layers:
         k, v = dw.step_kv(l)
-        dw.append_step(l, k, v)
-        ws.view(torch.int32).fill_(-1)
-        dw.decode(l, dw.step_q(l), ws, out)
-        outs[l] = out.cpu().numpy().copy()
+        qkv.append((dw.step_q(l), k, v))
+    if fused:
+        dw.decode(layers[0], qkv[0][0], ws, outs[0])   # read-only warm-up: first-call set-up outside the capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i, l in enumerate(layers):
+                q, k, v = qkv[i]
+                dw.decode_step(l, q, k, v, ws, outs[i])
+        g.replay()
+    else:
+        for i, l in enumerate(layers):
+            q, k, v = qkv[i]
+            dw.append_step(l, k, v)
+            ws.view(torch.int32).fill_(-1)
+            dw.decode(l, q, ws, outs[i])
     torch.cuda.synchronize()
-    return outs
+    host = outs.cpu().numpy()
+    return {l: host[i] for i, l in enumerate(layers)}
 
 
 def _check_lane(dw, wl, fmt, layer, lane, got, pages=(0, 1)):
@@ -69,24 +89,39 @@ def _check_lane(dw, wl, fmt, layer, lane, got, pages=(0, 1)):
 
 
 def test_batched_decode_27b_sampled():
-    """8 lanes x 40,960 tokens, 16 layers x 4 KV heads, 24 q heads; every layer's step run;
-    two (layer, lane) pairs compared in full against the oracle."""
+    """8 lanes x 40,960 tokens, 16 layers x 4 KV heads, 24 q heads, through the step the
+    benchmark times (every layer's kvq_decode_step in one CUDA graph, the step token closing page
+    639 of every lane); four (layer, lane) pairs compared in full against the oracle, with the
+    bytes of pages 0, 1 and the page the step closed, and the ring."""
     wl = synth.batched_decode_27b()
     dw = _dw(wl, HQ, fill=None)
     dw.fill_history([n - 1 for n in wl.seq_len])
     outs = _decode_step(dw, range(wl.num_layers))
     assert dw.cache.read_status() == 0
-    for layer, lane in ((0, 3), (15, 7)):
+    for layer, lane in ((0, 3), (5, 0), (10, 5), (15, 7)):
         _check_lane(dw, wl, HQ, layer, lane, outs[layer][lane])
     for l in range(wl.num_layers):
         assert np.all(np.isfinite(outs[l]))
+
+
+def test_batched_decode_27b_separate_calls_sampled():
+    """The same workload on two layers through kv_quant_append then paged_decode_attn (separate
+    calls, no kernel overlap); two (layer, lane) pairs against the oracle."""
+    wl = synth.batched_decode_27b(layers=2)
+    dw = _dw(wl, HQ, fill=None)
+    dw.fill_history([n - 1 for n in wl.seq_len])
+    outs = _decode_step(dw, range(wl.num_layers), fused=False)
+    assert dw.cache.read_status() == 0
+    for layer, lane in ((0, 6), (1, 2)):
+        _check_lane(dw, wl, HQ, layer, lane, outs[layer][lane])
 
 
 @pytest.mark.parametrize("fmt", [oracle.FMT_HQ2B_HAD, oracle.FMT_HQ2B_TOK, oracle.FMT_FP8])
 def test_batched_decode_27b_format_variants_sampled(fmt):
     """The 27B decode workload's per-layer sizes (8 lanes x 40,960 tokens, 4 KV heads, 24 q
     heads; two layers) in the rotated, per-token-K and FP8 formats, through the step the
-    benchmark times for them (append, then decode); two (layer, lane) pairs compared in full."""
+    benchmark times for them (kvq_decode_step in a CUDA graph); two (layer, lane) pairs compared
+    in full."""
     wl = synth.batched_decode_27b(layers=2)
     dw = _dw(wl, fmt, fill=None)
     dw.fill_history([n - 1 for n in wl.seq_len])
@@ -97,25 +132,43 @@ def test_batched_decode_27b_format_variants_sampled(fmt):
 
 
 def test_mixed_shared_prefix_window64_sampled():
-    """1 x 131,072 + 8 x 4,096 tokens whose first 2,048 live on 32 shared pages; W = 64."""
+    """1 x 131,072 + 8 x 4,096 tokens whose first 2,048 live on 32 shared pages; W = 64; every
+    layer's kvq_decode_step in one CUDA graph; four (layer, lane) pairs against the oracle."""
     wl = synth.mixed_shared_27b()
     dw = _dw(wl, HQ, fill=None)
     dw.fill_history([n - 1 for n in wl.seq_len])
-    layers = (0, 9)
-    outs = _decode_step(dw, layers)
+    outs = _decode_step(dw, range(wl.num_layers))
     assert dw.cache.read_status() == 0
     _check_lane(dw, wl, HQ, 0, 0, outs[0][0])
     _check_lane(dw, wl, HQ, 9, 4, outs[9][4])
+    _check_lane(dw, wl, HQ, 15, 1, outs[15][1])
     # the short lanes read the shared pages in place: lanes 2..8 never appended them
     _check_lane(dw, wl, HQ, 0, 8, outs[0][8], pages=(0, 31, 32))
 
 
+def _prefill_rows(chunk, group, extra=16, seed=0):
+    """Query rows of a chunk that meet every tile boundary of the tensor-core prefill (a CTA
+    takes 128 // group consecutive queries of one GQA group), the first and last rows, and a
+    seeded sample of the rest."""
+    qt = 128 // group
+    rows = {0, 1, chunk - 2, chunk - 1}
+    for t in range(qt, chunk, qt):
+        rows |= {t - 1, t}
+    rng = np.random.default_rng(seed)
+    rows |= set(int(x) for x in rng.choice(chunk, size=extra, replace=False))
+    return sorted(r for r in rows if 0 <= r < chunk)
+
+
 def test_chunked_prefill_65536_plus_1024_sampled():
-    """A 1,024-token chunk over a 65,536-token compressed prefix; garbage-filled workspace."""
+    """A 1,024-token chunk over a 65,536-token compressed prefix; garbage-filled workspace; on
+    layers 0, 7 and 15, every query row at a CTA tile boundary plus the first, last and a seeded
+    sample (> 100 rows of 24 heads) against the oracle."""
     wl = synth.chunked_prefill_27b()
     dw = _dw(wl, HQ, fill=None)
     prefix, chunk = 65536, 1024
-    layers = (0, 15)
+    layers = (0, 7, 15)
+    rows = _prefill_rows(chunk, wl.group)
+    assert len(rows) >= 64
     dw.fill_history([prefix], layers=layers)
     ws, out = dw.prefill_buffers(chunk)
     for l in layers:
@@ -128,11 +181,31 @@ def test_chunked_prefill_65536_plus_1024_sampled():
         got = out.cpu().numpy()
         assert dw.cache.read_status() == 0
         oc = LaneCache(wl, HQ, l, 0)
-        rows = [0, 1, 63, 64, 511, 1000, 1023]
         qh = wl.q_np(l, 0, prefix, chunk)[rows]
         ref = oc.attend(qh, [prefix + i for i in rows], 0, dw.sm_scale)
         assert_close(got[rows], ref, what=f"prefill layer {l}")
         assert np.all(np.isfinite(got))
+
+
+def test_prefill_prefix_over_three_splits_in_full():
+    """A 200-token chunk over a 20,000-token prefix: the keys span three 8,192-key splits, so
+    every query's result is a merge of three or more split partials; every row and head against
+    the oracle (one layer, 2 KV heads, GQA 6)."""
+    prefix, chunk = 20000, 200
+    n = prefix + chunk
+    wl = synth.Workload("prefill_3splits", 1, 2, 12, [n], np.arange((n + 63) // 64, dtype=np.int32)[None, :][:, ::-1]
+                        .copy(), (n + 63) // 64, window=0, seed=11)
+    dw = _dw(wl, HQ)
+    dw.fill_history([n])
+    ws, out = dw.prefill_buffers(chunk)
+    ws.view(torch.int32).fill_(-1)
+    q = wl.q_torch(0, 0, prefix, chunk, "cuda")
+    dw.prefill(0, q, [prefix], [chunk], [0], ws, out)
+    got = out.cpu().numpy()
+    assert dw.cache.read_status() == 0
+    oc = LaneCache(wl, HQ, 0, 0)
+    ref = oc.attend(wl.q_np(0, 0, prefix, chunk), [prefix + i for i in range(chunk)], 0, dw.sm_scale)
+    assert_close(got, ref, what="prefill over three splits")
 
 
 def test_needle_131072_hq_and_bf16():

@@ -376,3 +376,47 @@ def test_decode_step_equals_append_then_decode(fmt, window):
     assert torch.equal(A.cache.pool, B.cache.pool)
     assert (A.cache.ring is None) == (B.cache.ring is None)              # the FP8 format has no ring
     assert A.cache.ring is None or torch.equal(A.cache.ring, B.cache.ring)
+
+
+@pytest.mark.parametrize("call,fmt", [("decode", HQ), ("decode", TOK), ("decode", HAD), ("decode", FP8),
+                                      ("decode", BF), ("step", HQ), ("prefill", HQ), ("prefill", BF)])
+def test_lane_longer_than_max_seq_len_is_skipped(call, fmt):
+    """A lane whose seq_len exceeds the host bound max_seq_len (but not the page table) is
+    flagged BAD_LEN and skipped by every kernel of the call: no byte past the workspace the
+    bound sizes is touched, and the other lanes' results stay those of the oracle."""
+    from compressed_paged_kv_quant_gb300 import kvq
+    lens, bound = [200, 300], 256           # lane 1: 300 tokens, inside its 5-page table row
+    wl = _custom(lens, L=1, H=2, Hq=12)
+    dw = _dw(wl, fmt)
+    _gpu_fill(dw)
+    g, pool, ring = _oracle_full(wl, fmt)
+    ring_o = ring if fmt not in (BF, FP8) else None
+    guard = 1 << 16
+    if call == "prefill":
+        need = kvq.prefill_workspace_bytes(dw.g, 2, bound)
+    else:
+        need = kvq.decode_workspace_bytes(dw.g, 2, bound)
+    buf = torch.full((need + guard,), 0x5A, dtype=torch.uint8, device="cuda")
+    ws = buf[:need]
+    out = torch.full((2, 12, 256), 7.0, dtype=torch.float32, device="cuda")
+    if call == "prefill":
+        q = torch.cat([wl.q_torch(0, b, n - 1, 1, "cuda") for b, n in enumerate(lens)])
+        kvq.paged_prefill_attn(dw.g, 0, dw.cache.pool, dw.cache.ring, 0, dw.page_table,
+                               dw._i32([n - 1 for n in lens]), dw._i32([1, 1]), dw._i32([0, 1]), 1, dw.seq_len,
+                               bound, q, dw.sm_scale, ws, out, dw.cache.status)
+    elif call == "step":
+        # the step's token is the lane's last one, already in the cache: append it again
+        k, v = dw.step_kv(0)
+        kvq.kvq_decode_step(dw.g, 0, dw.cache.pool, dw.cache.ring, 0, dw.page_table, dw.step_start, dw.step_n,
+                            dw.step_off, k, v, dw.seq_len, bound, dw.step_q(0), dw.sm_scale, ws, out,
+                            dw.cache.status)
+    else:
+        kvq.paged_decode_attn(dw.g, 0, dw.cache.pool, dw.cache.ring, 0, dw.page_table, dw.seq_len, bound,
+                              dw.step_q(0), dw.sm_scale, ws, out, dw.cache.status)
+    torch.cuda.synchronize()
+    assert dw.cache.read_status() & kvq.STATUS_BAD_LEN
+    assert torch.all(buf[need:] == 0x5A), "bytes past the workspace were written"
+    qh = wl.q_np(0, 0, lens[0] - 1, 1)
+    ref, st = oracle.decode(g, 0, pool, ring_o, 0, wl.page_table[:1], 1, lens[:1], qh, dw.sm_scale)
+    assert st == 0
+    assert_close(out[:1].cpu().numpy(), ref, what=f"{call} fmt={fmt}: the valid lane")

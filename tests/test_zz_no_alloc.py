@@ -1,12 +1,13 @@
 """paged_decode_attn_noalloc against paged_decode_attn.
 
-Some callers cannot allocate device memory -- code inside a CUDA graph capture it does not
-own, plugins whose host engine's allocator owns the whole GPU.  The no-allocation entry point
-serves them from a static scratch array inside the library instead of a caller workspace.
-This test calls it through the C ABI twice in a row (with different queries, so a stale
-result from the first call cannot pass for the second) and checks each output against the
-regular entry point with a caller-allocated workspace, within the attention tolerance.
-It sits in a file of its own that pytest collects last.
+Some callers cannot allocate device memory -- plugins of a serving engine whose allocator
+owns the whole GPU and hands out no scratch, hosts that forbid allocation after start-up.
+The no-allocation entry point serves them from a static scratch array inside the library
+instead of a caller workspace.  This test first leaves partials of a larger call in that
+array (a wider split stride), then calls the entry point through the C ABI twice in a row
+(with different queries, so a stale result cannot pass for a fresh one) and checks each
+output against the regular entry point with a caller-allocated workspace, within the
+attention tolerance.  It sits in a file of its own that pytest collects last.
 """
 import numpy as np
 import pytest
@@ -37,6 +38,18 @@ def test_noalloc_decode_matches_workspace_decode():
     dw.fill_history(lens)
     ws, ref = dw.decode_buffers()
     out = torch.empty_like(ref)
+    # a larger call first: a page table four times as wide and a bound to match give every
+    # (lane, head) more split records, so the array is left holding non-zero partials laid
+    # out under another stride than the calls checked below
+    wide = torch.full((len(lens), 4 * max(pages)), -1, dtype=torch.int32, device="cuda")
+    wide[:, :max(pages)] = dw.page_table
+    wide_bound = 64 * wide.shape[1]
+    assert kvq.decode_workspace_bytes(dw.g, len(lens), wide_bound) > kvq.decode_workspace_bytes(
+        dw.g, len(lens), dw.max_seq_len)
+    kvq.paged_decode_attn_noalloc(dw.g, 1, dw.cache.pool, dw.cache.ring, wl.window, wide, dw.seq_len, wide_bound,
+                                  dw.step_q(1) * 3.0, dw.sm_scale, out, dw.cache.status)
+    torch.cuda.synchronize()
+    assert dw.cache.read_status() == 0
     for call, layer in enumerate((1, 0)):
         q = dw.step_q(layer) * (1.0 + call)          # a different query on each call
         dw.decode(layer, q, ws, ref)
