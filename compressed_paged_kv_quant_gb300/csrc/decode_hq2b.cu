@@ -27,10 +27,13 @@
 //     per-half sums instead.  The contraction order over the 256 dims is permuted so that each
 //     thread's A and B come from contiguous code bytes; a dot product does not depend on it.
 //   online softmax in FP32 (log2 domain) with a lazy rescale.
-//   O^T += V^ . P'^T: A = V codes of two tokens per fp16 pair (byte permute, LOP3, one HSUB2),
-//     B = P' = P (.) s_v (the per-token V scale folded into P, fp16) moved from the S^T
-//     accumulator layout to the B layout with movmatrix.trans; the zero points come back as
-//     sum P z in FP32.
+//   O^T += V^ . P'^T: A = V codes of two tokens per fp16 pair (byte permute, one AND: the code
+//     c at mantissa bits 2k, 2k + 1 with a zero exponent field is the fp16 subnormal c 2^(2k-24),
+//     exact, and the power of two comes off once at the end), B = P' = P (.) s_v (the per-token V
+//     scale folded into P, fp16).  P reaches the P.V warp already in the B layout (fp16, moved
+//     from the S^T accumulator layout with movmatrix.trans by the Q.K^T warp); one more MMA per
+//     16 tokens with A rows (z0, z1, s0, s1, 1) of the tokens' metadata and B = P gives
+//     sum P z per half, sum P s per half and sum P in FP32.
 #include "kvq_internal.cuh"
 #include "attn_args.cuh"
 #include "append_ops.cuh"
@@ -79,40 +82,33 @@ __device__ __forceinline__ uint32_t h2mul(uint32_t a, uint32_t b) {
 // is masked off and the exponent of M = 2^(10 - e - 2i) is OR-ed in (one LOP3); M + c is exact.
 //   keys:   e = 2 (the word shifted left by 2, or right by 6 for its high byte): M = 256, 64, 16,
 //           4; the MMA takes M + c as is and a per-page correction removes the M + 1.5 part.
-//   values, plain: e = 0 (the word as is, or shifted right by 8): M = 1024, 256, 64, 16; one
-//           HSUB2 (FMA pipe) of M turns M + c into the code c exactly.
-//   values, centred: e = 1 (the word shifted left by 1, or right by 7): M = 512, 128, 32, 8; one
-//           HSUB2 of M + 1.5 (exact in fp16 only for M <= 512) gives c - 1.5 exactly, and the
-//           zero point becomes z + 1.5 s.  The rotated format needs this: the fp16 rounding of
-//           P (.) s_v scales the whole code row, whose mean is 1.5, and the inverse rotation
-//           gathers that common part onto output dims 0 and 128; the centred row has mean ~0.
-//           It costs one shift per code word and one FMA per meta entry (~2% of a decode call),
-//           so the plain format keeps the first form.
+//   values: no exponent at all.  The word as is (low byte) or shifted right by 8 (high byte)
+//           leaves the code of position k at bits 2k, 2k + 1 of each half; masked (one AND) the
+//           half is the fp16 subnormal c 2^(2k - 24), exact, and the tensor core multiplies
+//           subnormals exactly.  Each O accumulator takes one position only, so its factor
+//           2^(2k - 24) comes off with one multiply when the partial is written.
+//           The rotated format subtracts 1.5 sum P' per half at the end (sum P' from one MMA
+//           with A = 1), which centres the codes: the fp16 rounding of P (.) s_v scales a whole
+//           code row, whose mean is 1.5, and the inverse rotation gathers that common part
+//           onto output dims 0 and 128; on centred rows it has mean ~0.
 __device__ __forceinline__ uint32_t lop_and_or(uint32_t x, uint32_t mask, uint32_t magic) {
   return (x & mask) | magic;
 }
-__device__ __forceinline__ uint32_t h2sub(uint32_t a, uint32_t b) {
-  __half2 r = __hsub2(*reinterpret_cast<__half2*>(&a), *reinterpret_cast<__half2*>(&b));
-  return *reinterpret_cast<uint32_t*>(&r);
-}
 constexpr uint32_t KMASK0 = 0x000C000Cu;   // key code position i: KMASK0 << 2i after the shift
-// value code position i: VMASK << 2i after the shift (plain, centred)
-constexpr uint32_t VMASK_PLAIN = 0x00030003u, VMASK_CENTRED = 0x00060006u;
-// fp16x2 bit patterns: M + 0 for keys (256, 64, 16, 4) and values (plain 1024, 256, 64, 16;
-// centred 512, 128, 32, 8), the key correction M + 1.5 (257.5, 65.5, 17.5, 5.5) and the value
-// centring M + 1.5 (513.5, 129.5, 33.5, 9.5), all exact in fp16
+constexpr uint32_t VMASK = 0x00030003u;    // value code position i: VMASK << 2i
+// fp16x2 bit patterns: M + 0 for keys (256, 64, 16, 4) and the key correction M + 1.5 (257.5,
+// 65.5, 17.5, 5.5), all exact in fp16
 __constant__ uint32_t c_kmag[4] = {0x5C005C00u, 0x54005400u, 0x4C004C00u, 0x44004400u};
 __constant__ uint32_t c_kcor[4] = {0x5C065C06u, 0x54185418u, 0x4C604C60u, 0x45804580u};
-__constant__ uint32_t c_vmag[4] = {0x64006400u, 0x5C005C00u, 0x54005400u, 0x4C004C00u};
-__constant__ uint32_t c_vmag_cen[4] = {0x60006000u, 0x58005800u, 0x50005000u, 0x48004800u};
-__constant__ uint32_t c_vcen[4] = {0x60036003u, 0x580C580Cu, 0x50305030u, 0x48C048C0u};
-
-// 1.5 s + c in float for a fp16 s (one mixed-precision FMA; 1.5 s is exact, so one rounding)
-__device__ __forceinline__ float fma_h15_f(uint16_t s, float c) {
-  float d;
-  asm("fma.rn.f32.f16 %0, %1, %2, %3;\n" : "=f"(d) : "h"(s), "h"((uint16_t)0x3E00u), "f"(c));
-  return d;
+// 2^(24 - 2k): the factor that turns an accumulator of subnormal codes at position k back into
+// codes
+__device__ __forceinline__ constexpr float vpos_scale(int k) {
+  return k == 0 ? 16777216.0f : k == 1 ? 4194304.0f : k == 2 ? 1048576.0f : 262144.0f;
 }
+
+__device__ __forceinline__ uint32_t shl2(uint32_t x) { return x << 2; }
+__device__ __forceinline__ uint32_t shr6(uint32_t x) { return x >> 6; }
+__device__ __forceinline__ uint32_t shr8(uint32_t x) { return x >> 8; }
 
 // lazy rescale: the running max of a head moves only when a page max exceeds it by more than
 // RESCALE_LOG2 (log2 domain), so P <= 2^0.5 and P * s_v stays below 65,504 for any finite V
@@ -148,9 +144,10 @@ __device__ __forceinline__ void cursor_next(Cursor& cu, const int* pre, int H) {
 }
 
 // Exchange slot written by the Q.K warp and read by the P.V warp of a pair, one page each:
-// per thread P[4 m-tiles][4] (fp32, C-fragment layout of S^T), then (alpha0, alpha1, m0, m1).
-// Stored as [5 float4][32 lanes] so both sides access it without bank conflicts.
-constexpr int X_F4 = 5;
+// per thread P of 4 m-tiles as fp16 B fragments (2 registers per m-tile: tokens 0-7 and 8-15
+// of the tile, for head r), then (alpha0, alpha1, m0, m1).  Stored as [3 uint4][32 lanes] so
+// both sides access it without bank conflicts.
+constexpr int X_F4 = 3;
 constexpr int X_BYTES = X_F4 * 32 * 16;
 constexpr int QS_BYTES = 8 * 32 * 16;   // the Q.K warp's query pairs: [8 uint4][32 lanes]
 constexpr int PAIR_BYTES = 4 * HQ2B_BLOCK + 2 * X_BYTES + QS_BYTES;  // K ring 2, V ring 2, exchange 2, q
@@ -168,11 +165,6 @@ __device__ __forceinline__ void locate(int u0, const int* pre, int lanes, int H,
   const int off = u0 - H * pre[lo];
   cu.h = off / cu.n;
   cu.p = off - cu.h * cu.n;
-}
-
-__device__ __forceinline__ bool page_phys(const CacheView& c, const Cursor& cu, int32_t& phys) {
-  phys = c.page_table[(int64_t)cu.b * c.max_pages + cu.p];
-  return phys >= 0 && phys < c.pool_pages;
 }
 
 // Warp pairs: warp w < DEC_PAIRS runs Q.K^T + softmax of a page, warp w + DEC_PAIRS runs its
@@ -257,10 +249,25 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
   uint8_t* ring = is_qk ? kring : vring;
   const int kv = is_qk ? 0 : 1;
   const int full_bar = is_qk ? PB_KFULL : PB_VFULL;
+  // physical pages of this warp's units, 32 at a time: lane l of chunk k holds the page of unit
+  // u0 + 32k + l (-1 past the range), so a page's copy waits on a page-table load only once per
+  // 32 pages
+  auto phys_chunk = [&](int k) -> int32_t {
+    const int u = u0 + 32 * k + lane;
+    int32_t ph = -1;
+    if (u < u1) {
+      Cursor t;
+      locate(u, pre, a.lanes, H, t);
+      ph = c.page_table[(int64_t)t.b * c.max_pages + t.p];
+    }
+    return ph;
+  };
+  int32_t ph_cur = phys_chunk(0);
   auto produce = [&]() {
     const int slot = produced & 1;
-    int32_t phys;
-    const bool ok = page_phys(c, pc, phys);
+    if ((produced & 31) == 0 && produced > 0) ph_cur = phys_chunk(produced >> 5);
+    const int32_t phys = __shfl_sync(0xFFFFFFFFu, ph_cur, produced & 31);
+    const bool ok = phys >= 0 && phys < c.pool_pages;
     if (ok) {
       // fused decode step: a page that the step's token closes (a main page only with window 0)
       // gets its K block and last V row from the append kernel this grid overlaps: wait for it
@@ -364,19 +371,18 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
       if (valid & (1u << slot)) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_KFULL + slot), par))) { timed_out = true; break; }
         const uint8_t* st = kring + slot * HQ2B_BLOCK;
-        float Cc[4] = {0.f, 0.f, 0.f, 0.f};   // sum over dims of q~ (M + 1.5): the same for every key
+        float Cc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // sum over dims of q~ (M + 1.5), in two chains
         float S1[4][4];                       // per-token-K: the second half's sums (S: the first)
 #pragma unroll
         for (int mt = 0; mt < 4; mt++)
 #pragma unroll
           for (int e = 0; e < 4; e++) S[mt][e] = S1[mt][e] = 0.f;
-        // k-step ks = 4j + i of thread column cq covers dims dim_base(cq, j) + {i, i+8} (A regs
-        // 0/1: codes of bytes 0/2 of word j) and {i+4, i+12} (A regs 2/3: bytes 1/3)
         const uint8_t* krow_a = st + perm_row(r) * HQ2B_ROW;
         const uint8_t* krow_b = st + (8 + perm_row(r)) * HQ2B_ROW;
+        // k-step ks = 4j + i of thread column cq covers dims dim_base(cq, j) + {i, i+8} (A regs
+        // 0/1: codes of bytes 0/2 of word j) and {i+4, i+12} (A regs 2/3: bytes 1/3)
 #pragma unroll
         for (int jw = 0; jw < 4; jw++) {
-          const int wbyte = dim_base<KTOK>(cq, jw) / 4;
           const uint4 qa = qsm[(2 * jw) * 32 + lane], qb = qsm[(2 * jw + 1) * 32 + lane];
           const uint32_t q0[4] = {qa.x, qa.y, qa.z, qa.w}, q1[4] = {qb.x, qb.y, qb.z, qb.w};
           uint32_t bq[4][2];
@@ -398,23 +404,35 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
               const uint32_t sel = (i & 1) ? 0x7632u : 0x5410u;
               bq[i][0] = h2mul(q0[i], __byte_perm(slo[i >> 1], shi[i >> 1], sel));
               bq[i][1] = h2mul(q1[i], __byte_perm(slo[2 + (i >> 1)], shi[2 + (i >> 1)], sel));
-              mma16816(Cc, kcor[i], kcor[i], kcor[i], kcor[i], bq[i][0], bq[i][1]);
+              mma16816(Cc[i & 1], kcor[i], kcor[i], kcor[i], kcor[i], bq[i][0], bq[i][1]);
             }
           }
+          // the code word of word jw (16 dims) of the thread's two key rows in every m-tile
+          const int wbyte = dim_base<KTOK>(cq, jw) / 4;
+          uint32_t la[4], ra[4], lb[4], rb[4];
 #pragma unroll
           for (int mt = 0; mt < 4; mt++) {
             const uint32_t wa = *reinterpret_cast<const uint32_t*>(krow_a + 16 * mt * HQ2B_ROW + wbyte);
             const uint32_t wb = *reinterpret_cast<const uint32_t*>(krow_b + 16 * mt * HQ2B_ROW + wbyte);
-            const uint32_t la = wa << 2, ra = wa >> 6, lb = wb << 2, rb = wb >> 6;
-            float(&acc)[4] = (KTOK && jw >= 2) ? S1[mt] : S[mt];
+            la[mt] = shl2(wa);
+            ra[mt] = shr6(wa);
+            lb[mt] = shl2(wb);
+            rb[mt] = shr6(wb);
+          }
+          // the four m-tiles' accumulators in turn, so that no MMA waits on the one before it
 #pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const uint32_t mk = KMASK0 << (2 * i);
-              mma16816(acc, lop_and_or(la, mk, kmag[i]), lop_and_or(lb, mk, kmag[i]), lop_and_or(ra, mk, kmag[i]),
-                       lop_and_or(rb, mk, kmag[i]), bq[i][0], bq[i][1]);
+          for (int i = 0; i < 4; i++) {
+            const uint32_t mk = KMASK0 << (2 * i);
+#pragma unroll
+            for (int mt = 0; mt < 4; mt++) {
+              float(&acc)[4] = (KTOK && jw >= 2) ? S1[mt] : S[mt];
+              mma16816(acc, lop_and_or(la[mt], mk, kmag[i]), lop_and_or(lb[mt], mk, kmag[i]),
+                       lop_and_or(ra[mt], mk, kmag[i]), lop_and_or(rb[mt], mk, kmag[i]), bq[i][0], bq[i][1]);
             }
           }
         }
+#pragma unroll
+        for (int e = 0; e < 4; e++) Cc[0][e] += Cc[1][e];
         if constexpr (KTOK) {
           // q . k^ = sum over halves of s (sum q (M + c) - sum q M) + z sum q, with the token's
           // own (s, z) per half, then the softmax scale (log2 domain)
@@ -437,7 +455,7 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
         } else {
           // q~ . k^ = 2 (sum q~ (M + c) - sum q~ (M + 1.5)), then the softmax scale (log2 domain)
           const float k2 = 2.f * sl2;
-          const float cn0 = -Cc[0] * k2, cn1 = -Cc[1] * k2;
+          const float cn0 = -Cc[0][0] * k2, cn1 = -Cc[0][1] * k2;
 #pragma unroll
           for (int mt = 0; mt < 4; mt++) {
             S[mt][0] = fmaf(S[mt][0], k2, cn0);
@@ -473,16 +491,21 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
         m1 = mx1;
       }
       const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
-      float4 px[4];
+      // P in fp16, moved from the S^T accumulator layout (token rows, head columns) to the B
+      // layout of the P.V step: thread (r, cq) gets head r of tokens 2cq, 2cq + 1 (QK rows) of
+      // each 8-token half of the m-tile
+      uint32_t pb[4][2];
 #pragma unroll
-      for (int mt = 0; mt < 4; mt++)
-        px[mt] = make_float4(ex2(S[mt][0] - mu0), ex2(S[mt][1] - mu1), ex2(S[mt][2] - mu0), ex2(S[mt][3] - mu1));
+      for (int mt = 0; mt < 4; mt++) {
+        pb[mt][0] = movmatrix_t(pack_h2(ex2(S[mt][0] - mu0), ex2(S[mt][1] - mu1)));
+        pb[mt][1] = movmatrix_t(pack_h2(ex2(S[mt][2] - mu0), ex2(S[mt][3] - mu1)));
+      }
       // ---- hand P, alpha and m to the P.V warp
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_XEMPTY + slot), par ^ 1u))) { timed_out = true; break; }
-      float4* xs = xring + slot * (X_F4 * 32);
-#pragma unroll
-      for (int mt = 0; mt < 4; mt++) xs[mt * 32 + lane] = px[mt];
-      xs[4 * 32 + lane] = make_float4(al0, al1, m0, m1);
+      uint4* xs = reinterpret_cast<uint4*>(xring + slot * (X_F4 * 32));
+      xs[lane] = make_uint4(pb[0][0], pb[0][1], pb[1][0], pb[1][1]);
+      xs[32 + lane] = make_uint4(pb[2][0], pb[2][1], pb[3][0], pb[3][1]);
+      reinterpret_cast<float4*>(xs)[64 + lane] = make_float4(al0, al1, m0, m1);
       __syncwarp();
       if (lane == 0) asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(BAR(PB_XFULL + slot)) : "memory");
       // next (lane, head) segment: fresh max, new query
@@ -498,70 +521,69 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
     }
   } else {
     // =========================================================== P.V warp
+    // O[8hf + i8]: rows = dims 128hf + 16r + 4(i8 >= 4) + (i8 & 3) and + 8, columns = heads
+    // 2cq, 2cq+1; accumulates subnormal codes of position i8 & 3 (factor 2^(2(i8&3) - 24)).
+    // Zm: rows (z0, z1, s0, s1, 1) x heads of the metadata MMA (thread row r holds row r);
+    // Cp[hf] (rotated format): row 0 = sum P' of half hf.
     float O[16][4];
-    float l0 = 0.f, l1 = 0.f, Z00 = 0.f, Z01 = 0.f, Z10 = 0.f, Z11 = 0.f;
+    float Zm[4] = {0.f, 0.f, 0.f, 0.f};
+    float Cp[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int i = 0; i < 16; i++)
 #pragma unroll
       for (int e = 0; e < 4; e++) O[i][e] = 0.f;
     const int t0 = perm_row(2 * cq), t1 = perm_row(2 * cq + 1);
-    uint32_t vmag[4], vcen[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) {
-      vmag[i] = CENTRED ? c_vmag_cen[i] : c_vmag[i];
-      vcen[i] = CENTRED ? c_vcen[i] : 0u;
-    }
+    // metadata pairs in the B layout: tokens (t0, t1) are the memory pair (2cq, 2cq+1), swapped
+    // for odd cq; low halves = s, high halves = z of a meta word
+    const uint32_t sel_s = (cq & 1) ? 0x1054u : 0x5410u, sel_z = (cq & 1) ? 0x3276u : 0x7632u;
+    // A of the metadata MMA, row r: z0 (r = 0), z1 (1), s0 (2), s1 (3), 1.0 (4), 0 (5-7)
+    const bool zy = r & 1;
+    const uint32_t zsel = r < 2 ? sel_z : sel_s;
+    const uint32_t zand = r < 4 ? 0xFFFFFFFFu : 0u, zor = r == 4 ? 0x3C003C00u : 0u;
+    const uint32_t ones_a = r == 0 ? 0x3C003C00u : 0u;   // A = 1 in row 0 (sum P', rotated format)
     for (int j = 0; j < n_units; j++) {
       const int slot = j & 1;
       const uint32_t par = (j >> 1) & 1;
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_XFULL + slot), par))) { timed_out = true; break; }
       // P of the page is read per m-tile below; the slot is released after the page
-      const float4* xs = xring + slot * (X_F4 * 32);
-      const float4 am = xs[4 * 32 + lane];
+      const uint4* xs = reinterpret_cast<const uint4*>(xring + slot * (X_F4 * 32));
+      const float4 am = reinterpret_cast<const float4*>(xs)[64 + lane];
       const float al0 = am.x, al1 = am.y;
-      l0 *= al0; l1 *= al1;
-      Z00 *= al0; Z10 *= al0; Z01 *= al1; Z11 *= al1;
       if (__any_sync(0xFFFFFFFFu, al0 != 1.0f || al1 != 1.0f)) {
 #pragma unroll
         for (int i = 0; i < 16; i++) {
           O[i][0] *= al0; O[i][1] *= al1; O[i][2] *= al0; O[i][3] *= al1;
         }
+        Zm[0] *= al0; Zm[1] *= al1;
+        if (CENTRED) {
+          Cp[0][0] *= al0; Cp[0][1] *= al1;
+          Cp[1][0] *= al0; Cp[1][1] *= al1;
+        }
       }
       if (valid & (1u << slot)) {
         if (!__all_sync(0xFFFFFFFFu, mbar_wait(BAR(PB_VFULL + slot), par))) { timed_out = true; break; }
         const uint8_t* st = vring + slot * HQ2B_BLOCK;
-        // per m-tile: P (.) s_v per half (fp16), sum(P z') (z' = z, or z + 1.5 s_v centred),
-        // sum(P), the B fragments, then O^T += V^ . P'^T with a fp16 pair holding one dim of two
-        // tokens as the exact code c (or c - 1.5 centred)
+        const uint4 pw0 = xs[lane], pw1 = xs[32 + lane];
+        const uint32_t pbs[4][2] = {{pw0.x, pw0.y}, {pw0.z, pw0.w}, {pw1.x, pw1.y}, {pw1.z, pw1.w}};
 #pragma unroll
         for (int mt = 0; mt < 4; mt++) {
-          const float4 pxm = xs[mt * 32 + lane];
-          const float pv[4] = {pxm.x, pxm.y, pxm.z, pxm.w};
-          uint32_t Bv[2][2];
+          // per 8-token half rr: the tokens' metadata, P' = P (.) s per half (fp16, B layout),
+          // and the metadata MMA's A row
+          uint32_t Bv[2][2], za[2];
 #pragma unroll
           for (int rr = 0; rr < 2; rr++) {
-            const int tok = 16 * mt + 8 * rr + perm_row(r);
-            const uint2 mw = *reinterpret_cast<const uint2*>(st + HQ2B_META_OFF + tok * 8);
-            float z0 = half_bits_to_float((uint16_t)(mw.x >> 16));
-            float z1 = half_bits_to_float((uint16_t)(mw.y >> 16));
-            if (CENTRED) {
-              z0 = fma_h15_f((uint16_t)(mw.x & 0xFFFFu), z0);
-              z1 = fma_h15_f((uint16_t)(mw.y & 0xFFFFu), z1);
-            }
-            const float pa = pv[2 * rr], pb = pv[2 * rr + 1];
-            l0 += pa;
-            l1 += pb;
-            Z00 = fmaf(pa, z0, Z00);
-            Z01 = fmaf(pb, z0, Z01);
-            Z10 = fmaf(pa, z1, Z10);
-            Z11 = fmaf(pb, z1, Z11);
-            const __half2 p2 = __floats2half2_rn(pa, pb);
-            const __half2 s0 = __low2half2(*reinterpret_cast<const __half2*>(&mw.x));
-            const __half2 s1 = __low2half2(*reinterpret_cast<const __half2*>(&mw.y));
-            const __half2 b0 = __hmul2(p2, s0), b1 = __hmul2(p2, s1);
-            Bv[0][rr] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&b0));
-            Bv[1][rr] = movmatrix_t(*reinterpret_cast<const uint32_t*>(&b1));
+            const uint4 u = *reinterpret_cast<const uint4*>(st + HQ2B_META_OFF + (16 * mt + 8 * rr + 2 * cq) * 8);
+            const uint32_t s0p = __byte_perm(u.x, u.z, sel_s), s1p = __byte_perm(u.y, u.w, sel_s);
+            Bv[0][rr] = h2mul(pbs[mt][rr], s0p);
+            Bv[1][rr] = h2mul(pbs[mt][rr], s1p);
+            za[rr] = (__byte_perm(zy ? u.y : u.x, zy ? u.w : u.z, zsel) & zand) | zor;
           }
+          mma16816(Zm, za[0], 0u, za[1], 0u, pbs[mt][0], pbs[mt][1]);
+          if (CENTRED) {
+            mma16816(Cp[0], ones_a, 0u, ones_a, 0u, Bv[0][0], Bv[0][1]);
+            mma16816(Cp[1], ones_a, 0u, ones_a, 0u, Bv[1][0], Bv[1][1]);
+          }
+          // O^T += V^ . P'^T, a fp16 pair holding one dim of two tokens as a subnormal code
 #pragma unroll
           for (int hf = 0; hf < 2; hf++) {
             const uint8_t* vb = st + 32 * hf + 4 * r;
@@ -571,21 +593,14 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
             const uint32_t w3 = *reinterpret_cast<const uint32_t*>(vb + (16 * mt + 8 + t1) * HQ2B_ROW);
             const uint32_t x[4] = {__byte_perm(w0, w1, 0x5410u), __byte_perm(w0, w1, 0x7632u),
                                    __byte_perm(w2, w3, 0x5410u), __byte_perm(w2, w3, 0x7632u)};
-            uint32_t lo[4], hi[4];
+            uint32_t hi[4];
 #pragma unroll
-            for (int k = 0; k < 4; k++) {
-              lo[k] = CENTRED ? x[k] << 1 : x[k];
-              hi[k] = x[k] >> (CENTRED ? 7 : 8);
-            }
+            for (int k = 0; k < 4; k++) hi[k] = shr8(x[k]);
 #pragma unroll
             for (int i8 = 0; i8 < 8; i8++) {
-              const int pos = i8 & 3;
-              const uint32_t* src = i8 < 4 ? lo : hi;
-              const uint32_t mk = (CENTRED ? VMASK_CENTRED : VMASK_PLAIN) << (2 * pos);
-              mma16816(O[8 * hf + i8], h2sub(lop_and_or(src[0], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]),
-                       h2sub(lop_and_or(src[1], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]),
-                       h2sub(lop_and_or(src[2], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]),
-                       h2sub(lop_and_or(src[3], mk, vmag[pos]), CENTRED ? vcen[pos] : vmag[pos]), Bv[hf][0], Bv[hf][1]);
+              const uint32_t* src = i8 < 4 ? x : hi;
+              const uint32_t mk = VMASK << (2 * (i8 & 3));
+              mma16816(O[8 * hf + i8], src[0] & mk, src[1] & mk, src[2] & mk, src[3] & mk, Bv[hf][0], Bv[hf][1]);
             }
           }
         }
@@ -596,15 +611,17 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
       // segment end: write this pair's partial (m, l, O + z-term) and start afresh
       const bool last = (j + 1 == n_units);
       if (last || cu.p + 1 == cu.n) {
-        float ls0 = l0, ls1 = l1, z00 = Z00, z01 = Z01, z10 = Z10, z11 = Z11;
+        // the metadata sums of heads 2cq, 2cq+1 live in thread rows 0-4 of this column
+        float zz[2][2], zs[2][2], ll[2], cp[2][2];
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          ls0 += __shfl_xor_sync(0xFFFFFFFFu, ls0, o);
-          ls1 += __shfl_xor_sync(0xFFFFFFFFu, ls1, o);
-          z00 += __shfl_xor_sync(0xFFFFFFFFu, z00, o);
-          z01 += __shfl_xor_sync(0xFFFFFFFFu, z01, o);
-          z10 += __shfl_xor_sync(0xFFFFFFFFu, z10, o);
-          z11 += __shfl_xor_sync(0xFFFFFFFFu, z11, o);
+        for (int e = 0; e < 2; e++) {
+          zz[0][e] = __shfl_sync(0xFFFFFFFFu, Zm[e], cq);
+          zz[1][e] = __shfl_sync(0xFFFFFFFFu, Zm[e], 4 + cq);
+          zs[0][e] = __shfl_sync(0xFFFFFFFFu, Zm[e], 8 + cq);
+          zs[1][e] = __shfl_sync(0xFFFFFFFFu, Zm[e], 12 + cq);
+          ll[e] = __shfl_sync(0xFFFFFFFFu, Zm[e], 16 + cq);
+          cp[0][e] = __shfl_sync(0xFFFFFFFFu, Cp[0][e], cq);
+          cp[1][e] = __shfl_sync(0xFFFFFFFFu, Cp[1][e], cq);
         }
         const int segstart = H * pre[cu.b] + cu.h * (pre[cu.b + 1] - pre[cu.b]);
         const int k = gp - segstart / Wp;
@@ -616,19 +633,20 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
             float* dst = a.ws_o + pidx * D;
 #pragma unroll
             for (int hf = 0; hf < 2; hf++) {
-              const float z = hf == 0 ? (e == 0 ? z00 : z01) : (e == 0 ? z10 : z11);
+              // the zero points: sum P z (plain); sum P (z + 1.5 s) - 1.5 sum P' (centred codes)
+              const float z = CENTRED ? fmaf(1.5f, zs[hf][e] - cp[hf][e], zz[hf][e]) : zz[hf][e];
               float v[16];
 #pragma unroll
               for (int i = 0; i < 8; i++) {
-                v[i] = O[8 * hf + i][e] + z;
-                v[8 + i] = O[8 * hf + i][2 + e] + z;
+                v[i] = fmaf(O[8 * hf + i][e], vpos_scale(i & 3), z);
+                v[8 + i] = fmaf(O[8 * hf + i][2 + e], vpos_scale(i & 3), z);
               }
               float4* d4 = reinterpret_cast<float4*>(dst + 128 * hf + 16 * r);
 #pragma unroll
               for (int i = 0; i < 4; i++) d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
             }
             if (r == 0)
-              reinterpret_cast<float2*>(a.ws_ml)[pidx] = e == 0 ? make_float2(am.z, ls0) : make_float2(am.w, ls1);
+              reinterpret_cast<float2*>(a.ws_ml)[pidx] = e == 0 ? make_float2(am.z, ll[0]) : make_float2(am.w, ll[1]);
           }
         }
         if (!last) {
@@ -637,7 +655,11 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
           for (int i = 0; i < 16; i++)
 #pragma unroll
             for (int e = 0; e < 4; e++) O[i][e] = 0.f;
-          l0 = l1 = Z00 = Z01 = Z10 = Z11 = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; e++) {
+            Zm[e] = 0.f;
+            Cp[0][e] = Cp[1][e] = 0.f;
+          }
         }
       } else {
         cursor_next(cu, pre, H);
