@@ -121,8 +121,9 @@ class Clocks:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"bench_clocks_{os.getpid()}.csv")
+            import tempfile
+            fd, self.path = tempfile.mkstemp(prefix="kvq_bench_clocks_", suffix=".csv")
+            os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -157,9 +158,14 @@ class Clocks:
                         reasons.add(n)
         except Exception:
             return None
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "window": "warm-up, timed decode steps, per-call timing and the end-to-end steps"}
 
 
 def _device_index():
@@ -233,9 +239,15 @@ def run_reference(args):
         od.run(1)
     secs = [od.run(per_step) for _ in range(args.steps)]
     value = od.value(per_step * args.steps, sum(secs))
+    lane_layer_ms = 1000.0 * sum(secs) / (per_step * args.steps)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * WORKLOAD["lanes"] * WORKLOAD["ctx"] / value,
+            "measured": {"lane_layer_ms": lane_layer_ms, "lane_layers_timed": per_step * args.steps,
+                         "seconds": round(sum(secs), 2),
+                         "ms_per_step_is": (f"derived: the measured lane-layer time x {WORKLOAD['lanes']} lanes x "
+                                            f"{od.wl.num_layers} layers (one lane of the 8 was timed, through all "
+                                            "16 layers' worth of decodes on one layer's cache)")},
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": _config(),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": od.threads, "kind": "oracle",
@@ -310,12 +322,12 @@ def run_gpu(args):
         torch.cuda.synchronize()
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = Clocks()
+    clocks.start()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             g.replay()
     barrier()
-    clocks = Clocks()
-    clocks.start()
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(args.steps):
@@ -323,7 +335,6 @@ def run_gpu(args):
         e1.record(stream)
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
-    clk = clocks.stop()
     ms = max_over_ranks(ms, world, dev)
     assert dw.cache.read_status() == 0, "device status flagged during the timed steps"
     tokens_per_step = lanes * ctx
@@ -374,9 +385,14 @@ def run_gpu(args):
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
     e2e_value = job_throughput(world, tokens_per_step, e2e_ms)
+    clk = clocks.stop()
 
     moves = None if args.no_page_moves else run_page_moves(dw, stream)
+    del dw, step_in, step_out, ws
+    torch.cuda.empty_cache()
     prefill = None if (args.no_prefill or args.format != "hq2b") else run_prefill(args, dev, stream)
+    mixed = None if (args.no_legs or args.format != "hq2b") else run_mixed(args, dev, stream)
+    needle = None if (args.no_legs or args.format != "hq2b") else run_needle(args, dev, stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -384,7 +400,13 @@ def run_gpu(args):
         od.run(1)
         dt = od.run(args.cpu_repeats)
         cpu = {"value": od.value(args.cpu_repeats, dt), "unit": UNIT, "cores": od.threads, "kind": "oracle",
-               "sample": od.describe(args.cpu_repeats), "seconds": round(dt, 2)}
+               "sample": od.describe(args.cpu_repeats), "seconds": round(dt, 2),
+               "lane_layer_ms": 1000.0 * dt / args.cpu_repeats}
+        od.threads = 1
+        r1 = max(1, args.cpu_repeats // 16)
+        dt1 = od.run(r1)
+        cpu["one_core"] = {"value": od.value(r1, dt1), "unit": UNIT, "cores": 1, "sample": od.describe(r1),
+                           "seconds": round(dt1, 2), "lane_layer_ms": 1000.0 * dt1 / r1}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -410,6 +432,8 @@ def run_gpu(args):
                 "gpu_launches": (4 if args.format == "hq2b_had" else 3) * L * args.steps,
                 "clocks": clk,
                 "prefill": prefill,
+                "mixed_shared_prefix": mixed,
+                "needle_hq2b_and_bf16": needle,
                 "page_moves": moves}
         print(json.dumps(line))
     if world > 1:
@@ -456,6 +480,113 @@ def run_page_moves(dw, stream, reps=5):
             "gather_device_to_device_gbs": gbs(g_d, 2),
             "memcpy_device_to_host_gbs": gbs(c_dh), "memcpy_host_to_device_gbs": gbs(c_hd),
             "note": "device-to-device counts read + write bytes; host legs count the bytes moved"}
+
+
+def _graph_ms(stream, fn, reps, warm=3):
+    """ms per replay of one CUDA graph of fn() (run once eagerly first), CUDA events on the stream."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_mixed(args, dev, stream):
+    """The mixed pool with shared prefixes (1 x 131,072 + 8 x 4,096 tokens, the short lanes'
+    first 2,048 tokens on 32 shared pages, window 64): one decode step per layer through
+    kvq_decode_step in one CUDA graph, and the attention call alone.  GB/s on the unique
+    compressed bytes (pages in the pool) and on the logical ones (every lane's tokens)."""
+    import torch
+
+    from compressed_paged_kv_quant_gb300 import kvq, synth
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+    wl = synth.mixed_shared_27b(layers=args.layers)
+    L, H = wl.num_layers, wl.num_kv_heads
+    with torch.cuda.stream(stream):
+        dw = DeviceWorkload(wl, kvq.FMT_HQ2B, dev, fill=None, stream=stream.cuda_stream)
+        dw.fill_history([n - 1 for n in wl.seq_len], chunk=16384)
+        qs = [dw.step_q(l) for l in range(L)]
+        kvs = [dw.step_kv(l) for l in range(L)]
+        ws, _ = dw.decode_buffers()
+        outs = torch.empty((L, wl.lanes, wl.num_q_heads, 256), dtype=torch.float32, device=dev)
+    stream.synchronize()
+
+    def step():
+        for l in range(L):
+            dw.decode_step(l, qs[l], kvs[l][0], kvs[l][1], ws, outs[l])
+
+    def attn():
+        for l in range(L):
+            dw.decode(l, qs[l], ws, outs[l])
+
+    reps = max(10, args.steps // 4)
+    step_ms = _graph_ms(stream, step, reps)
+    call_ms = _graph_ms(stream, attn, reps) / L
+    assert dw.cache.read_status() == 0, "device status flagged in the mixed-pool leg"
+    unique = wl.pool_pages * 64 * H * KV_BYTES["hq2b"]
+    logical = sum(wl.seq_len) * H * KV_BYTES["hq2b"]
+    peak, _ = _peaks()
+    gbs = lambda b: b / (call_ms / 1e3) / 1e9
+    return {"workload": "mixed_27b: 1 x 131,072 + 8 x 4,096 tokens (first 2,048 of the short lanes on 32 shared "
+                        f"pages), window 64, {L} layers, 4 KV heads, 24 q heads, 2-bit pages",
+            "ms_per_step": step_ms, "ms_per_attention_call": call_ms,
+            "unique_bytes_per_layer": unique, "logical_bytes_per_layer": logical,
+            "gbs_unique": gbs(unique), "gbs_logical": gbs(logical), "frac_unique": gbs(unique) / peak,
+            "context_tokens_per_s": sum(wl.seq_len) / (step_ms / 1e3),
+            "l2_policy": f"inputs larger than L2 ({unique * L / 1e9:.2f} GB of pages per step)"}
+
+
+def run_needle(args, dev, stream, reps=30):
+    """The needle workload (1 layer, 4 KV heads, 24 q heads, 131,072 tokens): one attention call
+    over the 2-bit pool (75.5 MB, smaller than L2) and over the BF16 pool (537 MB), L2 flushed by
+    a 256 MB write before every timed call; CUDA events around each call."""
+    import torch
+
+    from compressed_paged_kv_quant_gb300 import kvq, synth
+    from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
+    wl = synth.needle_131k()
+    n, H = wl.seq_len[0], wl.num_kv_heads
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    peak, _ = _peaks()
+    res = {"workload": "needle_131072: 1 layer, 4 KV heads, 24 q heads, 131,072 tokens, one needle",
+           "l2_policy": "256 MB buffer written before every timed call"}
+    for fmt in ("hq2b", "bf16"):
+        with torch.cuda.stream(stream):
+            dw = DeviceWorkload(wl, getattr(kvq, FORMATS[fmt]), dev, fill=None, stream=stream.cuda_stream)
+            dw.fill_history([n], chunk=16384)
+            q = dw.step_q(0)
+            ws, out = dw.decode_buffers()
+            for _ in range(3):
+                dw.decode(0, q, ws, out)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in ev:
+                flush.fill_(1)
+                e0.record(stream)
+                dw.decode(0, q, ws, out)
+                e1.record(stream)
+        stream.synchronize()
+        assert dw.cache.read_status() == 0, "device status flagged in the needle leg"
+        ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+        nbytes = n * H * KV_BYTES[fmt]
+        res[fmt] = {"ms_per_attention_call": ms, "bytes": nbytes, "gbs": nbytes / (ms / 1e3) / 1e9,
+                    "frac": nbytes / (ms / 1e3) / 1e9 / peak}
+        del dw
+        torch.cuda.empty_cache()
+    res["hq2b_over_bf16_time"] = res["hq2b"]["ms_per_attention_call"] / res["bf16"]["ms_per_attention_call"]
+    return res
 
 
 def prefill_flops(prefix, chunk, q_heads):
@@ -551,6 +682,9 @@ def main():
                          "hq2b_tok (K per token), fp8 (E4M3) or bf16 (the exact reference path); the "
                          "variants time decode only")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-legs", action="store_true", help="skip the mixed-pool and needle legs")
+    ap.add_argument("--leg", default=None, choices=["mixed", "needle", "prefill"],
+                    help="run one leg alone and print its JSON (for profiling)")
     ap.add_argument("--no-page-moves", action="store_true")
     ap.add_argument("--step-calls", default="fused", choices=["fused", "separate"],
                     help="one kvq_decode_step per layer, or kv_quant_append + paged_decode_attn")
@@ -559,7 +693,23 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.leg:
+        return run_leg(args)
     return run_gpu(args)
+
+
+def run_leg(args):
+    """One leg alone on cuda:0 (a smaller command to profile under ncu)."""
+    import torch
+
+    from compressed_paged_kv_quant_gb300 import build
+    build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    fn = {"mixed": run_mixed, "needle": run_needle, "prefill": run_prefill}[args.leg]
+    print(json.dumps({"leg": args.leg, "result": fn(args, dev, stream)}))
+    return 0
 
 
 if __name__ == "__main__":

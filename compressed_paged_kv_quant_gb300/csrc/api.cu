@@ -13,6 +13,7 @@ struct AttnArgs;
 int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t stream);
 int launch_decode_hq2b(const AttnArgs& a, cudaStream_t stream);
 int launch_decode_fp8(const AttnArgs& a, cudaStream_t stream);
+int launch_decode_bf16(const AttnArgs& a, cudaStream_t stream);
 int decode_split_tokens(int fmt);
 int prefill_split_tokens(int fmt);
 int decode_hq2b_slots(int max_seq_len);
@@ -228,7 +229,7 @@ int paged_decode_attn(const kvq_geom* g, int layer, const void* pool, size_t poo
   }
   if (two_bit(g->format)) return launch_decode_hq2b(a, (cudaStream_t)stream);
   if (g->format == KVQ_FMT_FP8) return launch_decode_fp8(a, (cudaStream_t)stream);
-  return launch_attn_generic(g->format, a, 1, (cudaStream_t)stream);
+  return launch_decode_bf16(a, (cudaStream_t)stream);
 }
 
 int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,

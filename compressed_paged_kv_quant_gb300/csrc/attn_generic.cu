@@ -185,7 +185,10 @@ __global__ void __launch_bounds__(256) attn_combine(AttnArgs a, int decode, int 
 }
 
 int decode_split_tokens(int fmt) {
-  return fmt == KVQ_FMT_HQ2B ? DECODE_SPLIT_HQ2B : fmt == KVQ_FMT_FP8 ? DECODE_SPLIT_FP8 : GENERIC_SPLIT;
+  return fmt == KVQ_FMT_HQ2B ? DECODE_SPLIT_HQ2B
+         : fmt == KVQ_FMT_FP8  ? DECODE_SPLIT_FP8
+         : fmt == KVQ_FMT_BF16 ? DECODE_SPLIT_BF16
+                               : GENERIC_SPLIT;
 }
 int prefill_split_tokens(int) { return PREFILL_SPLIT; }
 

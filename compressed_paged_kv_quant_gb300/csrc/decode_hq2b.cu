@@ -49,8 +49,12 @@ namespace kvq {
 #endif
 constexpr int DEC_PAIRS = KVQ_DEC_PAIRS;               // warp pairs per CTA
 constexpr int DEC_CTAS_PER_SM = KVQ_DEC_CTAS_PER_SM;  // resident CTAs per SM the grid is sized for
-constexpr int MIN_PAGES_PER_WARP = 2;
-constexpr int DEC_MAX_SLOTS = 96;            // partial records per (lane, query head), at most
+// A pair takes at least MIN_PAGES_PER_WARP pages, and a (lane, head) segment writes at most
+// DEC_MAX_SLOTS partial records: a single long lane (131,072 tokens, 2,048 pages a head) is still
+// cut into ranges of 9 pages, enough to keep every pair of the grid busy, while 8 lanes of 40,960
+// tokens need 162 records a (lane, query head), 32 MB of workspace.
+constexpr int MIN_PAGES_PER_WARP = 4;
+constexpr int DEC_MAX_SLOTS = 256;           // partial records per (lane, query head), at most
 
 // pages of lane b handled by the MMA path (everything before its exact tail); a lane whose
 // length is unusable has none, and *err (if given) receives its status bits

@@ -25,6 +25,7 @@ constexpr int MAX_GROUP = 8;
 constexpr int GENERIC_SPLIT = 1024;   // decode, generic kernel
 constexpr int DECODE_SPLIT_HQ2B = 1024;
 constexpr int DECODE_SPLIT_FP8 = 1024;    // tokens per CTA of the FP8 decode kernel
+constexpr int DECODE_SPLIT_BF16 = 1024;   // tokens per CTA of the BF16 decode kernel
 constexpr int PREFILL_SPLIT = 8192;
 
 __host__ __device__ constexpr int block_bytes(int fmt) {

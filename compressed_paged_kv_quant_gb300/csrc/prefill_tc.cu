@@ -15,7 +15,7 @@
 //                        O [256,512) fp32 accumulator of the split.
 //   Shared memory:       K tile x2 (64 keys x 256 dims fp16, 128B-swizzled, K-major B of S),
 //                        V tile x2 (the same [key][dim] layout, read as the MN-major B of PV),
-//                        compressed-page staging x2 (one 9,216 B TMA bulk copy per page).
+//                        compressed-page staging x PT_NSTG (one 9,216 B TMA bulk copy per page).
 //   Warps 0-3: softmax, one row per thread (= TMEM lane): S from TMEM, causal mask, online
 //              max with lazy O rescale (only when a row max grows by more than 2^8), P to
 //              TMEM, l in FP32; the epilogue writes (m, l, O) of the split.
@@ -34,22 +34,22 @@ constexpr int PT_DQ_WARPS = 7;                    // TMA + dequantisation warps 
 constexpr int PT_MMA_WARP = 4 + PT_DQ_WARPS;      // the warp whose lane 0 issues the MMAs
 constexpr int PT_THREADS = (PT_MMA_WARP + 1) * 32;
 constexpr int PT_STAGE = 2 * HQ2B_BLOCK;  // compressed K + V block of one page (one layer/head)
+constexpr int PT_NSTG = 6;                // compressed pages in flight per CTA
 constexpr int SM_K = 0;                   // 2 x 32 KB
 constexpr int SM_V = 65536;               // 2 x 32 KB
-constexpr int SM_STG = 131072;            // 2 x 9,216 B
-constexpr int SM_BAR = SM_STG + 2 * PT_STAGE;
-constexpr int NUM_BARS = 17;
+constexpr int SM_STG = 131072;            // PT_NSTG x 9,216 B
+constexpr int SM_BAR = SM_STG + PT_NSTG * PT_STAGE;
+constexpr int NUM_BARS = 2 * PT_NSTG + 13;
 constexpr int SM_ABORT = SM_BAR + NUM_BARS * 8;
 constexpr int SM_TMEM = SM_ABORT + 4;
 constexpr int PT_SMEM = SM_TMEM + 12 + 1024;  // + slack to align the base to 1,024 B
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr int PT_SPIN = 1 << 16;
-constexpr int PT_POLL = 1 << 22;   // MMA-issuer polls (20 ns sleep each): ~0.1 s before giving up
 constexpr float RESCALE_LOG2 = 8.0f;
 
 enum {
-  B_STG_FULL = 0, B_STG_EMPTY = 2, B_K_FULL = 4, B_K_EMPTY = 6, B_V_FULL = 8,
-  B_S_FULL = 10, B_P_FULL = 12, B_PV_DONE = 14, B_Q_READY = 16
+  B_K_FULL = 0, B_K_EMPTY = 2, B_V_FULL = 4, B_S_FULL = 6, B_P_FULL = 8, B_PV_DONE = 10, B_Q_READY = 12,
+  B_STG_FULL = 13, B_STG_EMPTY = 13 + PT_NSTG
 };
 
 __device__ __forceinline__ uint32_t sm_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -59,15 +59,6 @@ __device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void bar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool bar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
   for (int i = 0; i < PT_SPIN; i++) {
@@ -229,9 +220,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
   auto BAR = [&](int i) { return sm_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; i++) {
+    for (int i = 0; i < PT_NSTG; i++) {
       bar_init(BAR(B_STG_FULL + i), 1);
       bar_init(BAR(B_STG_EMPTY + i), PT_DQ_WARPS);
+    }
+    for (int i = 0; i < 2; i++) {
       bar_init(BAR(B_K_FULL + i), PT_DQ_WARPS);
       bar_init(BAR(B_K_EMPTY + i), 1);
       bar_init(BAR(B_V_FULL + i), PT_DQ_WARPS);
@@ -404,8 +397,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
     constexpr int DQ_T = 32 * PT_DQ_WARPS;
     const int64_t lane_row = (int64_t)b * c.max_pages;
     auto issue = [&](int j) -> bool {
-      const int buf = j & 1;
-      if (!bar_wait(BAR(B_STG_EMPTY + buf), ((j >> 1) & 1) ^ 1)) return false;
+      const int buf = j % PT_NSTG;
+      if (!bar_wait(BAR(B_STG_EMPTY + buf), ((j / PT_NSTG) & 1) ^ 1)) return false;
       const int32_t phys = c.page_table[lane_row + p0 + j];
       if (phys < 0 || phys >= c.pool_pages) {
         flag(c.status, KVQ_STATUS_PAGE_OOB);
@@ -426,7 +419,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
     };
     int issued = 0;
     if (tid == 0) {
-      for (; issued < 2 && issued < ntiles; issued++)
+      for (; issued < PT_NSTG && issued < ntiles; issued++)
         if (!issue(issued)) { timed_out = true; break; }
     }
     const __half2 two = __float2half2_rn(2.0f), m11 = __float2half2_rn(-11.0f);
@@ -442,8 +435,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       const int buf = j & 1;
       const uint32_t par = (j >> 1) & 1;
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) { timed_out = true; break; }
-      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_STG_FULL + buf), par))) { timed_out = true; break; }
-      const uint32_t stg = sm_u32(smem + SM_STG + buf * PT_STAGE);
+      const int sbuf = j % PT_NSTG;
+      if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_STG_FULL + sbuf), (j / PT_NSTG) & 1))) { timed_out = true; break; }
+      const uint32_t stg = sm_u32(smem + SM_STG + sbuf * PT_STAGE);
       const int key0 = (p0 + j) * P;
       // ---- K tile (B of S, K-major): k^ = s_d (2c - 3)
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_K_EMPTY + buf), par ^ 1))) { timed_out = true; break; }
@@ -510,7 +504,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       __syncwarp();
       if (lane == 0) {
         bar_arrive(BAR(B_V_FULL + buf));
-        bar_arrive(BAR(B_STG_EMPTY + buf));
+        bar_arrive(BAR(B_STG_EMPTY + sbuf));
       }
       if (tid == 0 && issued < ntiles) {
         if (!issue(issued)) timed_out = true;
@@ -520,7 +514,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
     }
     // copies still in flight must land before the CTA exits
     if (tid == 0) {
-      for (int j = max(0, issued - 2); j < issued; j++) bar_wait(BAR(B_STG_FULL + (j & 1)), (j >> 1) & 1);
+      for (int j = max(0, issued - PT_NSTG); j < issued; j++) bar_wait(BAR(B_STG_FULL + j % PT_NSTG), (j / PT_NSTG) & 1);
     }
   } else {
     // =============================================================== MMA warp (one thread)
@@ -555,30 +549,22 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
         ok = bar_wait(BAR(B_K_FULL), 0);
         if (ok) issue_s(0);
       }
-      // Per tile j: S(j+1) once its K tile is ready and PV(j) once P(j) and the V tile are;
-      // whichever is ready first goes first (S(j+1) preferred), so a late dequant does not hold
-      // back PV(j) and a late softmax does not hold back S(j+1).  S(j+1) reuses the S/P buffer of
-      // tile j-1, whose PV was issued in the previous round.
+      // Per tile j: S(j+1) once its K tile is ready, then PV(j) once P(j) and the V tile are.
+      // S(j+1) reuses the S/P buffer of tile j-1, whose PV was issued in the previous round (the
+      // MMAs run in issue order).  The waits suspend the thread (no polling), so the issuer takes
+      // no issue slots from the dequantisation and softmax warps while it waits.
       for (int j = 0; j < ntiles && ok; j++) {
-        if (*abort_flag) { ok = false; break; }
         const int buf = j & 1;
         const uint32_t par = (j >> 1) & 1;
-        bool s_done = j + 1 >= ntiles, pv_done = false;
-        for (int spin = 0; !(s_done && pv_done); spin++) {
-          if (spin > PT_POLL) { ok = false; break; }
-          if (!s_done && bar_test(BAR(B_K_FULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1)) {
-            issue_s(j + 1);
-            s_done = true;
-            continue;
-          }
-          if (!pv_done && bar_test(BAR(B_P_FULL + buf), par) && bar_test(BAR(B_V_FULL + buf), par)) {
-            issue_pv(j);
-            last_pv = j;
-            pv_done = true;
-            continue;
-          }
-          __nanosleep(20);
+        if (j + 1 < ntiles) {
+          ok = bar_wait(BAR(B_K_FULL + ((j + 1) & 1)), ((j + 1) >> 1) & 1) && !*abort_flag;
+          if (!ok) break;
+          issue_s(j + 1);
         }
+        ok = bar_wait(BAR(B_P_FULL + buf), par) && bar_wait(BAR(B_V_FULL + buf), par) && !*abort_flag;
+        if (!ok) break;
+        issue_pv(j);
+        last_pv = j;
       }
       if (!ok) {
         timed_out = true;

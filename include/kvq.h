@@ -259,7 +259,7 @@ int kvq_pages_scatter(const kvq_geom* geom, void* pool, size_t pool_bytes, const
  *   process exits.  The call allocates nothing and calls no allocating routine.
  *   Limit: kvq_decode_workspace_bytes(geom, lanes, max_seq_len) must not exceed
  *   KVQ_NOALLOC_SCRATCH_BYTES, else KVQ_ERR_SCRATCH_LIMIT and nothing is launched (at the
- *   27B geometry that is room for 8 lanes x 40,960 tokens several times over).  Every other
+ *   27B geometry that is room for 8 lanes x 40,960 tokens, 30.6 MiB of partials).  Every other
  *   argument is checked first, with the codes paged_decode_attn returns.
  *   The first call on a device looks up the array's device address (once per device, with
  *   that device current); make that first call before any stream capture.

@@ -223,18 +223,22 @@ def test_decode_ragged_lanes(fmt, window):
     assert dw.cache.read_status() == 0
 
 
+@pytest.mark.parametrize("fmt", [HQ, BF, FP8])
 @pytest.mark.parametrize("G", [1, 2, 3, 5, 7, 8])
-def test_decode_group_sizes(G):
+def test_decode_group_sizes(G, fmt):
+    """Every GQA group size the kernels take (heads padded to 8 in the tensor-core tiles)."""
     lens = [333, 1100]
     wl = _custom(lens, L=1, H=2, Hq=2 * G)
-    dw = _dw(wl, HQ)
+    dw = _dw(wl, fmt)
     _gpu_fill(dw)
-    g, pool, ring = _oracle_full(wl, HQ)
+    g, pool, ring = _oracle_full(wl, fmt)
     ws, out = dw.decode_buffers()
+    ws.view(torch.int32).fill_(-1)
     dw.decode(0, dw.step_q(0), ws, out)
     qh = np.concatenate([wl.q_np(0, b, n - 1, 1) for b, n in enumerate(lens)])
-    ref, _ = oracle.decode(g, 0, pool, ring, 0, wl.page_table, 2, lens, qh, dw.sm_scale)
-    assert_close(out.cpu().numpy(), ref, what=f"G={G}")
+    ref, _ = oracle.decode(g, 0, pool, ring if fmt == HQ else None, 0, wl.page_table, 2, lens, qh, dw.sm_scale)
+    assert_close(out.cpu().numpy(), ref, what=f"fmt={fmt} G={G}")
+    assert dw.cache.read_status() == 0
 
 
 def test_decode_zero_length_lane_gives_zeros():
