@@ -391,6 +391,13 @@ def run_gpu(args):
     del dw, step_in, step_out, ws
     torch.cuda.empty_cache()
     prefill = None if (args.no_prefill or args.format != "hq2b") else run_prefill(args, dev, stream)
+    prefill_fmts = None
+    if not (args.no_prefill or args.no_legs or args.format != "hq2b"):
+        prefill_fmts = {}
+        for f in ("hq2b_tok", "hq2b_had", "fp8"):
+            r = run_prefill(args, dev, stream, fmt=f, layers=1, steps=2)
+            prefill_fmts[f] = {k: r[k] for k in ("ms_per_layer_attention", "tflops", "roofline")}
+            torch.cuda.empty_cache()
     mixed = None if (args.no_legs or args.format != "hq2b") else run_mixed(args, dev, stream)
     needle = None if (args.no_legs or args.format != "hq2b") else run_needle(args, dev, stream)
 
@@ -432,6 +439,7 @@ def run_gpu(args):
                 "gpu_launches": (4 if args.format == "hq2b_had" else 3) * L * args.steps,
                 "clocks": clk,
                 "prefill": prefill,
+                "prefill_format_variants": prefill_fmts,
                 "mixed_shared_prefix": mixed,
                 "needle_hq2b_and_bf16": needle,
                 "page_moves": moves}
@@ -595,7 +603,7 @@ def prefill_flops(prefix, chunk, q_heads):
     return 4.0 * 256 * pairs * q_heads
 
 
-def run_prefill(args, dev, stream):
+def run_prefill(args, dev, stream, fmt="hq2b", layers=None, steps=None):
     """Chunked prefill over a compressed prefix (65,536 + 1,024 tokens, 16 layers): each layer
     appends the chunk's K/V, then paged_prefill_attn with a garbage-filled workspace."""
     import torch
@@ -603,10 +611,10 @@ def run_prefill(args, dev, stream):
     from compressed_paged_kv_quant_gb300 import kvq, synth
     from compressed_paged_kv_quant_gb300.workload import DeviceWorkload
     prefix, chunk = args.prefill_prefix, 1024
-    wl = synth.chunked_prefill_27b(prefix=prefix, chunk=chunk, layers=args.layers)
+    wl = synth.chunked_prefill_27b(prefix=prefix, chunk=chunk, layers=layers or args.layers)
     L = wl.num_layers
     with torch.cuda.stream(stream):
-        dw = DeviceWorkload(wl, kvq.FMT_HQ2B, dev, fill=None, stream=stream.cuda_stream)
+        dw = DeviceWorkload(wl, getattr(kvq, FORMATS[fmt]), dev, fill=None, stream=stream.cuda_stream)
         dw.fill_history([prefix], chunk=16384)
         ks = [wl.kv_torch(l, 0, prefix, chunk, 0, dev) for l in range(L)]
         vs = [wl.kv_torch(l, 0, prefix, chunk, 1, dev) for l in range(L)]
@@ -636,7 +644,7 @@ def run_prefill(args, dev, stream):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     call_ms = []
-    steps = max(2, args.prefill_steps)
+    steps = max(2, steps or args.prefill_steps)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(steps):
@@ -656,7 +664,8 @@ def run_prefill(args, dev, stream):
     except Exception:
         pass
     tflops = flops / (ms / 1000.0) / 1e12
-    return {"workload": f"prefill_27b: {chunk}-token chunk over a {prefix}-token 2-bit prefix, {L} layers, 24 q heads",
+    return {"workload": f"prefill_27b: {chunk}-token chunk over a {prefix}-token prefix, {L} layers, 24 q heads, "
+                        f"{fmt} pages",
             "ms_per_layer_attention": ms, "ms_per_step": step_ms, "flop_per_layer": flops, "tflops": tflops,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "peak_source": "measured bf16 dense (fp16 MMA runs at the same rate)"},
@@ -707,8 +716,11 @@ def run_leg(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    fn = {"mixed": run_mixed, "needle": run_needle, "prefill": run_prefill}[args.leg]
-    print(json.dumps({"leg": args.leg, "result": fn(args, dev, stream)}))
+    if args.leg == "prefill":
+        res = run_prefill(args, dev, stream, fmt=args.format if args.format != "bf16" else "hq2b")
+    else:
+        res = {"mixed": run_mixed, "needle": run_needle}[args.leg](args, dev, stream)
+    print(json.dumps({"leg": args.leg, "result": res}))
     return 0
 
 

@@ -17,7 +17,7 @@ int launch_decode_bf16(const AttnArgs& a, cudaStream_t stream);
 int decode_split_tokens(int fmt);
 int prefill_split_tokens(int fmt);
 int decode_hq2b_slots(int max_seq_len);
-int launch_prefill_hq2b_tc(const AttnArgs& a, cudaStream_t stream);
+int launch_prefill_tc(int fmt, const AttnArgs& a, cudaStream_t stream);
 int launch_attn_combine(const AttnArgs& a, int decode, cudaStream_t stream);
 int launch_page_move(uint8_t* pool, uint8_t* arena, const int32_t* page_ids, int n_pages, int64_t page_bytes,
                      int64_t pool_pages, int gather, int32_t* status, cudaStream_t stream);
@@ -240,7 +240,6 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
   int rc = check_attn_common(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
                              max_seq_len, q, workspace, out, d_status, true);
   if (rc) return rc;
-  if (g->format == KVQ_FMT_HQ2B_HAD) return KVQ_ERR_UNSUPPORTED;   // no rotated prefill kernel
   if (max_n_q < 0 || n_q_rows < 0) return KVQ_ERR_INVALID_ARG;
   if (lanes == 0 || max_n_q == 0) return KVQ_OK;
   if (!q_pos0 || !n_q || !q_offset) return KVQ_ERR_INVALID_ARG;
@@ -264,13 +263,12 @@ int paged_prefill_attn(const kvq_geom* g, int layer, const void* pool, size_t po
   a.grid_warps = 0;
   a.min_wp = 0;
   a.max_seq_len = max_seq_len;
-  if (g->format == KVQ_FMT_HQ2B) {
-    rc = launch_prefill_hq2b_tc(a, (cudaStream_t)stream);
-    return rc ? rc : launch_attn_combine(a, 0, (cudaStream_t)stream);
-  }
-  // BF16 pages, and the per-token-K format (its keys scale per token, which the tensor-core
-  // prefill's per-channel K tile does not): the CUDA-core split kernel
-  return launch_attn_generic(layout_fmt(g->format), a, 0, (cudaStream_t)stream);
+  if (g->format == KVQ_FMT_BF16)   // the exact reference pages: the CUDA-core split kernel
+    return launch_attn_generic(KVQ_FMT_BF16, a, 0, (cudaStream_t)stream);
+  // (the rotated format's prefill turns its page rows back to the original basis itself: q and
+  // the output need no rotation)
+  rc = launch_prefill_tc(g->format, a, (cudaStream_t)stream);
+  return rc ? rc : launch_attn_combine(a, 0, (cudaStream_t)stream);
 }
 
 int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes, void* ring, int window,

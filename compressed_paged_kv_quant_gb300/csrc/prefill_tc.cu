@@ -33,23 +33,39 @@ constexpr int PT_ROWS = 128;
 constexpr int PT_DQ_WARPS = 7;                    // TMA + dequantisation warps (12 warps: <= 168 regs)
 constexpr int PT_MMA_WARP = 4 + PT_DQ_WARPS;      // the warp whose lane 0 issues the MMAs
 constexpr int PT_THREADS = (PT_MMA_WARP + 1) * 32;
-constexpr int PT_STAGE = 2 * HQ2B_BLOCK;  // compressed K + V block of one page (one layer/head)
-constexpr int PT_NSTG = 6;                // compressed pages in flight per CTA
-constexpr int SM_K = 0;                   // 2 x 32 KB
-constexpr int SM_V = 65536;               // 2 x 32 KB
-constexpr int SM_STG = 131072;            // PT_NSTG x 9,216 B
-constexpr int SM_BAR = SM_STG + PT_NSTG * PT_STAGE;
-constexpr int NUM_BARS = 2 * PT_NSTG + 13;
-constexpr int SM_ABORT = SM_BAR + NUM_BARS * 8;
-constexpr int SM_TMEM = SM_ABORT + 4;
-constexpr int PT_SMEM = SM_TMEM + 12 + 1024;  // + slack to align the base to 1,024 B
+constexpr int SM_K = 0;                   // 2 K tile buffers
+
+// Per page format.  The staging ring holds a page's K and V blocks of one (layer, head) as one
+// bulk copy a stage: 9,216 B for the 2-bit layouts (6 stages), 32 KB for FP8 (2 stages).  Two
+// formats keep the K tile as two fp16 parts (hi, lo), 64 KB a buffer (3 stages): the per-token-K
+// format (its keys z + c s sit on a grid set by the token's largest values, too coarse for one
+// fp16) and the rotated format (its keys are turned back by H in the dequantisation, so every
+// element is a sum that one fp16 would round).  The rotated format turns its value rows back
+// as well, so q and the output stay in the original basis.
+template <int FMT>
+struct PfLayout {
+  static constexpr int LFMT = FMT == KVQ_FMT_FP8 ? KVQ_FMT_FP8 : KVQ_FMT_HQ2B;   // byte layout
+  static constexpr bool KSPLIT = FMT == KVQ_FMT_HQ2B_TOK || FMT == KVQ_FMT_HQ2B_HAD;
+  static constexpr bool VSPLIT = false;
+  static constexpr int K_BUF = KSPLIT ? 65536 : 32768;   // one K tile buffer (hi, then lo)
+  static constexpr int V_BUF = VSPLIT ? 65536 : 32768;   // one V tile buffer (hi, then lo)
+  static constexpr int SM_V = 2 * K_BUF;
+  static constexpr int SM_STG = SM_V + 2 * V_BUF;
+  static constexpr int STAGE = 2 * block_bytes(LFMT);
+  static constexpr int NSTG = LFMT == KVQ_FMT_FP8 ? 2 : (KSPLIT || VSPLIT) ? 3 : 6;
+  static constexpr int SM_BAR = SM_STG + NSTG * STAGE;
+  static constexpr int NUM_BARS = 13 + 2 * NSTG;
+  static constexpr int SM_ABORT = SM_BAR + NUM_BARS * 8;
+  static constexpr int SM_TMEM = SM_ABORT + 4;
+  static constexpr int SMEM = SM_TMEM + 12 + 1024;   // + slack to align the base to 1,024 B
+};
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr int PT_SPIN = 1 << 16;
 constexpr float RESCALE_LOG2 = 8.0f;
 
 enum {
   B_K_FULL = 0, B_K_EMPTY = 2, B_V_FULL = 4, B_S_FULL = 6, B_P_FULL = 8, B_PV_DONE = 10, B_Q_READY = 12,
-  B_STG_FULL = 13, B_STG_EMPTY = 13 + PT_NSTG
+  B_STG_FULL = 13   // then NSTG "full" and NSTG "empty" barriers of the staging ring
 };
 
 __device__ __forceinline__ uint32_t sm_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -179,14 +195,26 @@ __device__ __forceinline__ void dq_pairs(uint32_t lo, uint32_t hi, uint32_t (&x)
   x[3] = ((hi * 0x00040010u) & 0x03000300u) | 0x44004400u;
 }
 
+// two E4M3 bytes (low 16 bits) -> fp16 pair, exact
+__device__ __forceinline__ uint32_t e4m3x2_h2(uint32_t x) {
+  uint32_t y;
+  asm("{\n .reg .b16 t;\n cvt.u16.u32 t, %1;\n cvt.rn.f16x2.e4m3x2 %0, t;\n}\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 
 // ---------------------------------------------------------------------------- kernel
-// grid (splits, ceil(max_n_q / QT), lanes * H); PT_THREADS threads; PT_SMEM dynamic smem
-__global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
+// grid (splits, ceil(max_n_q / QT), lanes * H); PT_THREADS threads; PfLayout<FMT>::SMEM dynamic smem
+template <int FMT>
+__global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
+  using LY = PfLayout<FMT>;
+  constexpr int PT_STAGE = LY::STAGE, PT_NSTG = LY::NSTG;
+  constexpr int B_STG_EMPTY = B_STG_FULL + PT_NSTG;
+  constexpr bool FP8 = LY::LFMT == KVQ_FMT_FP8;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
@@ -211,12 +239,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
   const int k1 = min(k0 + a.split_tokens, kmax);
   const int p0 = k0 / P;
   const int ntiles = (k1 + P - 1) / P - p0;
-  const int ef = exact_from(len, c.window, c.ktok);
+  // first key read exact from the ring (FP8 pages have no ring: every key from its page)
+  const int ef = FP8 ? len : exact_from(len, c.window, c.ktok);
 
   uint8_t* smem = smem_raw + ((1024u - (sm_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM_BAR);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM_ABORT);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM_TMEM);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::SM_BAR);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::SM_ABORT);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::SM_TMEM);
   auto BAR = [&](int i) { return sm_u32(&bars[i]); };
 
   if (threadIdx.x == 0) {
@@ -253,6 +282,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
     const bool row_valid = row < QT * G && q_first + qi < nq;
     const int qpos = qpos0 + q_first + qi;
     const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+    // softmax scale (log2 domain); FP8 pages: times the K scale, E4M3 values being unscaled in the tile
+    const float sl2 = FP8 ? a.scale_log2 * c.k_scale : a.scale_log2;
     // Q row -> TMEM columns [0,128) as fp16 pairs
     for (int ch = 0; ch < 4; ch++) {
       uint32_t r[32];
@@ -305,13 +336,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
 #pragma unroll
         for (int cidx = 0; cidx < 64; cidx++) {
           const bool ok = row_valid && key0 + cidx <= qpos;
-          const float x = ok ? __uint_as_float(sv[cidx]) * a.scale_log2 : -INFINITY;
+          const float x = ok ? __uint_as_float(sv[cidx]) * sl2 : -INFINITY;
           sv[cidx] = __float_as_uint(x);
           t8[cidx & 7] = fmaxf(t8[cidx & 7], x);
         }
       }
       float tmax = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
-      if (full) tmax *= a.scale_log2;
+      if (full) tmax *= sl2;
       const float m_new = fmaxf(m_run, tmax);
       const bool first = (j == 0) || (m_run == -INFINITY);
       const bool need = !first && (m_new > m_run + RESCALE_LOG2);
@@ -344,7 +375,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
 #pragma unroll
       for (int i = 0; i < 8; i++) ps[i] = 0.f;
       if (full) {
-        const float sc = a.scale_log2, nm = -m_use;
+        const float sc = sl2, nm = -m_use;
 #pragma unroll
         for (int i = 0; i < 32; i++) {
           const float e0 = ex2f(fmaf(__uint_as_float(sv[2 * i]), sc, nm));
@@ -377,6 +408,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
     if (!timed_out) {
       tc_fence_after();
       const int64_t pidx = ((int64_t)(qoff + q_first + qi) * Hq + h * G + g) * a.max_splits + s;
+      const float vsc = FP8 ? c.v_scale : 1.0f;   // FP8 pages: the V scale, E4M3 values being unscaled
       for (int ch = 0; ch < 8; ch++) {
         uint32_t o[32];
         TC_LD32(tl + TM_O + 32 * ch, o);
@@ -385,8 +417,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
           float4* dst = reinterpret_cast<float4*>(a.ws_o + pidx * D + 32 * ch);
 #pragma unroll
           for (int i = 0; i < 8; i++)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                 __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * vsc, __uint_as_float(o[4 * i + 1]) * vsc,
+                                 __uint_as_float(o[4 * i + 2]) * vsc, __uint_as_float(o[4 * i + 3]) * vsc);
         }
       }
       if (row_valid) reinterpret_cast<float2*>(a.ws_ml)[pidx] = make_float2(m_run, l_run);
@@ -405,8 +437,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
         bar_arrive(BAR(B_STG_FULL + buf));
         return true;
       }
-      const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
-      const uint32_t dst = sm_u32(smem + SM_STG + buf * PT_STAGE);
+      const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(LY::LFMT, H, c.layer, h, 0);
+      const uint32_t dst = sm_u32(smem + LY::SM_STG + buf * PT_STAGE);
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(BAR(B_STG_FULL + buf)),
                    "r"((uint32_t)PT_STAGE)
@@ -437,28 +469,82 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) { timed_out = true; break; }
       const int sbuf = j % PT_NSTG;
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_STG_FULL + sbuf), (j / PT_NSTG) & 1))) { timed_out = true; break; }
-      const uint32_t stg = sm_u32(smem + SM_STG + sbuf * PT_STAGE);
+      const uint32_t stg = sm_u32(smem + LY::SM_STG + sbuf * PT_STAGE);
       const int key0 = (p0 + j) * P;
-      // ---- K tile (B of S, K-major): k^ = s_d (2c - 3)
+      // ---- K tile (B of S, K-major): k^ = s_d (2c - 3) (per channel), z + c s (per-token-K
+      // format), the E4M3 value (FP8; its scale multiplies the scores); keys from the ring as
+      // they are, turned by H in the rotated format (a warp holds one key row, 8 dims a lane)
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_K_EMPTY + buf), par ^ 1))) { timed_out = true; break; }
-      const uint32_t kb = sm_u32(smem + SM_K + buf * 32768) + tile_off;
+      const uint32_t kb = sm_u32(smem + SM_K + buf * LY::K_BUF) + tile_off;
       {
-        const uint4 sc = ld_shared_v4(stg + HQ2B_META_OFF + 16 * cc);
-        const uint32_t scs[4] = {sc.x, sc.y, sc.z, sc.w};
-        if (key0 + P <= ef) {   // every key of the tile comes from the codes (ef <= len)
-#pragma unroll 2
-          for (int t = t0; t < P; t += KSTEP) {
-            uint32_t res[4];
+        uint32_t scs[4] = {0u, 0u, 0u, 0u};
+        if constexpr (!FP8 && FMT != KVQ_FMT_HQ2B_TOK) {
+          const uint4 sc = ld_shared_v4(stg + HQ2B_META_OFF + 16 * cc);
+          scs[0] = sc.x; scs[1] = sc.y; scs[2] = sc.z; scs[3] = sc.w;
+        }
+        // codes (or E4M3 bytes) of key t, dims 8cc .. 8cc + 7 -> 4 fp16 pairs
+        auto key_code = [&](int t) -> uint4 {
+          uint32_t res[4];
+          if constexpr (FP8) {
+            const uint32_t w0 = ld_shared_u32(stg + t * D + 8 * cc), w1 = ld_shared_u32(stg + t * D + 8 * cc + 4);
+            res[0] = e4m3x2_h2(w0); res[1] = e4m3x2_h2(w0 >> 16); res[2] = e4m3x2_h2(w1); res[3] = e4m3x2_h2(w1 >> 16);
+          } else if constexpr (FMT == KVQ_FMT_HQ2B_TOK) {
+            res[0] = res[1] = res[2] = res[3] = 0u;   // (the split path below writes this format's tile)
+          } else {
             dq_pairs(ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc), ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1), res);
 #pragma unroll
             for (int p = 0; p < 4; p++) res[p] = h2u(__hmul2(__hfma2(u2h(res[p]), two, m11), u2h(scs[p])));
-            st_shared_v4(kb + swz(t, cc & 7), make_uint4(res[0], res[1], res[2], res[3]));
           }
+          return make_uint4(res[0], res[1], res[2], res[3]);
+        };
+        // per-token-K format: k^ = z + c s exactly in fp32 (one rounding at most), stored as the fp16
+        // pair hi = fp16(k^), lo = fp16(k^ - hi), in the two halves of the K buffer
+        // (rotated format: the key's rotated coordinates s_d (2c - 3) turned back by H, a warp per
+        // key row, lane cc holding dims 8cc .. 8cc + 7)
+        auto key_split = [&](int t, uint4& hi, uint4& lo) {
+          const uint32_t code = ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc) | (ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1) << 8);
+          float v[8];
+          if constexpr (FMT == KVQ_FMT_HQ2B_HAD) {
+#pragma unroll
+            for (int p = 0; p < 4; p++) {
+              const float2 sp = __half22float2(u2h(scs[p]));
+              v[2 * p] = sp.x * (float)(2 * (int)((code >> (4 * p)) & 3u) - 3);
+              v[2 * p + 1] = sp.y * (float)(2 * (int)((code >> (4 * p + 2)) & 3u) - 3);
+            }
+            warp_fwht256(v);
+          } else {
+            const uint32_t meta = ld_shared_u32(stg + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+            const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu)), zf = half_bits_to_float((uint16_t)(meta >> 16));
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
+          }
+          uint32_t h[4], l[4];
+#pragma unroll
+          for (int p = 0; p < 4; p++) {
+            const __half2 hh = __floats2half2_rn(v[2 * p], v[2 * p + 1]);
+            const float2 hf = __half22float2(hh);
+            h[p] = h2u(hh);
+            l[p] = h2u(__floats2half2_rn(v[2 * p] - hf.x, v[2 * p + 1] - hf.y));
+          }
+          hi = make_uint4(h[0], h[1], h[2], h[3]);
+          lo = make_uint4(l[0], l[1], l[2], l[3]);
+        };
+        if (LY::KSPLIT && key0 + P <= ef) {
+#pragma unroll 2
+          for (int t = t0; t < P; t += KSTEP) {
+            uint4 hi, lo;
+            key_split(t, hi, lo);
+            st_shared_v4(kb + swz(t, cc & 7), hi);
+            st_shared_v4(kb + 32768 + swz(t, cc & 7), lo);
+          }
+        } else if (key0 + P <= ef) {   // every key of the tile comes from the page (ef <= len)
+#pragma unroll 2
+          for (int t = t0; t < P; t += KSTEP) st_shared_v4(kb + swz(t, cc & 7), key_code(t));
         } else
 #pragma unroll 2
         for (int t = t0; t < P; t += KSTEP) {
           const int kp = key0 + t;
-          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          uint4 o = make_uint4(0u, 0u, 0u, 0u), olo = make_uint4(0u, 0u, 0u, 0u);
           if (kp < len) {
             if (kp >= ef) {
               const uint4 w = reinterpret_cast<const uint4*>(
@@ -467,15 +553,14 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
               o.y = h2u(__floats2half2_rn(bf16_lo(w.y), bf16_hi(w.y)));
               o.z = h2u(__floats2half2_rn(bf16_lo(w.z), bf16_hi(w.z)));
               o.w = h2u(__floats2half2_rn(bf16_lo(w.w), bf16_hi(w.w)));
+            } else if constexpr (LY::KSPLIT) {
+              key_split(t, o, olo);
             } else {
-              uint32_t res[4];
-              dq_pairs(ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc), ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1), res);
-#pragma unroll
-              for (int p = 0; p < 4; p++) res[p] = h2u(__hmul2(__hfma2(u2h(res[p]), two, m11), u2h(scs[p])));
-              o = make_uint4(res[0], res[1], res[2], res[3]);
+              o = key_code(t);
             }
           }
           st_shared_v4(kb + swz(t, cc & 7), o);
+          if constexpr (LY::KSPLIT) st_shared_v4(kb + 32768 + swz(t, cc & 7), olo);
         }
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
@@ -483,22 +568,41 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       if (lane == 0) bar_arrive(BAR(B_K_FULL + buf));
       // ---- V tile (B of PV, MN-major): v^ = z + c s, one rounding, per token and 128-dim half
       if (!__all_sync(0xFFFFFFFFu, bar_wait(BAR(B_PV_DONE + buf), par ^ 1))) { timed_out = true; break; }
-      const uint32_t vb = sm_u32(smem + SM_V + buf * 32768) + tile_off;
-      const uint32_t vst = stg + HQ2B_BLOCK;
+      const uint32_t vb = sm_u32(smem + LY::SM_V + buf * LY::V_BUF) + tile_off;
+      const uint32_t vst = stg + block_bytes(LY::LFMT);
       const bool vall = key0 + P <= len;
 #pragma unroll 2
       for (int t = t0; t < P; t += KSTEP) {
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        uint4 o = make_uint4(0u, 0u, 0u, 0u), olo = make_uint4(0u, 0u, 0u, 0u);
         if (vall || key0 + t < len) {
-          const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
-          const __half2 s2 = u2h(__byte_perm(meta, 0u, 0x1010u)), z2 = u2h(__byte_perm(meta, 0u, 0x3232u));
-          uint32_t res[4];
-          dq_pairs(ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc), ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1), res);
+          if constexpr (FP8) {
+            const uint32_t w0 = ld_shared_u32(vst + t * D + 8 * cc), w1 = ld_shared_u32(vst + t * D + 8 * cc + 4);
+            o = make_uint4(e4m3x2_h2(w0), e4m3x2_h2(w0 >> 16), e4m3x2_h2(w1), e4m3x2_h2(w1 >> 16));
+          } else if constexpr (FMT == KVQ_FMT_HQ2B_HAD) {
+            // v^ = H (z + c s): the rotated row dequantized in fp32, turned back by the warp
+            const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+            const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
+            const float zf = half_bits_to_float((uint16_t)(meta >> 16));
+            const uint32_t code =
+                ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc) | (ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1) << 8);
+            float v[8];
 #pragma unroll
-          for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
-          o = make_uint4(res[0], res[1], res[2], res[3]);
+            for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
+            warp_fwht256(v);
+            o = make_uint4(h2u(__floats2half2_rn(v[0], v[1])), h2u(__floats2half2_rn(v[2], v[3])),
+                           h2u(__floats2half2_rn(v[4], v[5])), h2u(__floats2half2_rn(v[6], v[7])));
+          } else {
+            const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+            const __half2 s2 = u2h(__byte_perm(meta, 0u, 0x1010u)), z2 = u2h(__byte_perm(meta, 0u, 0x3232u));
+            uint32_t res[4];
+            dq_pairs(ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc), ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1), res);
+#pragma unroll
+            for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
+            o = make_uint4(res[0], res[1], res[2], res[3]);
+          }
         }
         st_shared_v4(vb + swz(t, cc & 7), o);
+        if constexpr (LY::VSPLIT) st_shared_v4(vb + 32768 + swz(t, cc & 7), olo);
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       __syncwarp();
@@ -526,22 +630,34 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
       auto issue_s = [&](int j) {
         const int buf = j & 1;
         tc_fence_after();
-        const uint32_t kb = sm_u32(smem + SM_K + buf * 32768);
+        const uint32_t kb = sm_u32(smem + SM_K + buf * LY::K_BUF);
 #pragma unroll
         for (int ks = 0; ks < 16; ks++)
           tc_mma_ts(tmem + TM_S0 + 64 * buf, tmem + TM_Q + 8 * ks, sw128_desc(kb + (ks >> 2) * 8192 + (ks & 3) * 32),
                     IDESC_S, ks > 0);
+        if constexpr (LY::KSPLIT) {   // + Q . K_lo^T: the low parts of the keys
+#pragma unroll
+          for (int ks = 0; ks < 16; ks++)
+            tc_mma_ts(tmem + TM_S0 + 64 * buf, tmem + TM_Q + 8 * ks,
+                      sw128_desc(kb + 32768 + (ks >> 2) * 8192 + (ks & 3) * 32), IDESC_S, 1u);
+        }
         tc_commit(BAR(B_S_FULL + buf));
         tc_commit(BAR(B_K_EMPTY + buf));
       };
       auto issue_pv = [&](int j) {
         const int buf = j & 1;
         tc_fence_after();
-        const uint32_t vb = sm_u32(smem + SM_V + buf * 32768);
+        const uint32_t vb = sm_u32(smem + LY::SM_V + buf * LY::V_BUF);
 #pragma unroll
         for (int ks = 0; ks < 4; ks++)
           tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_mn_desc(vb + 2048 * ks), IDESC_PV,
                     (j > 0 || ks > 0) ? 1u : 0u);
+        if constexpr (LY::VSPLIT) {   // + P . V_lo: the low parts of the values
+#pragma unroll
+          for (int ks = 0; ks < 4; ks++)
+            tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_mn_desc(vb + 32768 + 2048 * ks), IDESC_PV,
+                      1u);
+        }
         tc_commit(BAR(B_PV_DONE + buf));
       };
       int last_pv = -1;
@@ -587,19 +703,31 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_hq2b_tc(AttnArgs a) {
   }
 }
 
-int launch_prefill_hq2b_tc(const AttnArgs& a, cudaStream_t stream) {
+template <int FMT>
+static int launch_prefill_fmt(const AttnArgs& a, cudaStream_t stream) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
   if (!attr_set[dev]) {
-    cudaFuncSetAttribute(prefill_hq2b_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, PT_SMEM);
+    cudaFuncSetAttribute(prefill_tc<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfLayout<FMT>::SMEM);
     attr_set[dev] = true;
   }
   const int QT = PT_ROWS / a.c.group;
   dim3 grid(a.max_splits, (a.max_n_q + QT - 1) / QT, a.lanes * a.c.num_kv_heads);
-  prefill_hq2b_tc<<<grid, PT_THREADS, PT_SMEM, stream>>>(a);
+  prefill_tc<FMT><<<grid, PT_THREADS, PfLayout<FMT>::SMEM, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+// The tensor-core prefill of every compressed format: fmt is the geometry's format.
+int launch_prefill_tc(int fmt, const AttnArgs& a, cudaStream_t stream) {
+  switch (fmt) {
+    case KVQ_FMT_HQ2B: return launch_prefill_fmt<KVQ_FMT_HQ2B>(a, stream);
+    case KVQ_FMT_HQ2B_HAD: return launch_prefill_fmt<KVQ_FMT_HQ2B_HAD>(a, stream);
+    case KVQ_FMT_HQ2B_TOK: return launch_prefill_fmt<KVQ_FMT_HQ2B_TOK>(a, stream);
+    case KVQ_FMT_FP8: return launch_prefill_fmt<KVQ_FMT_FP8>(a, stream);
+    default: return KVQ_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace kvq

@@ -49,17 +49,16 @@ typedef struct CUstream_st* kvq_stream_t; /* same handle as cudaStream_t; NULL =
  * h = 1, 2, ..., 128, pairs (a + b, a - b), then x 1/16), so codes are reproducible bit for bit.
  * The ring keeps keys as they came.  Decode rotates the query (q.k = Hq.Hk) and turns the output
  * back (sum p Hv = H sum p v), so results approximate the same attention as HQ2B.
- * kv_quant_append, paged_decode_attn (and _noalloc), kvq_decode_step and the page moves take it;
- * paged_prefill_attn returns KVQ_ERR_UNSUPPORTED for it.  Its decode workspace is larger by
- * lanes * num_q_heads * 512 B (the rotated query); kvq_decode_workspace_bytes counts it. */
+ * Every call takes it.  Its decode workspace is larger by lanes * num_q_heads * 512 B (the
+ * rotated query); kvq_decode_workspace_bytes counts it.  Its prefill turns the page rows back to
+ * the original basis before the tensor-core products, so q and the output are never rotated. */
 /* KVQ_FMT_HQ2B_TOK: the HQ2B byte layout with each K row coded when it is appended, per token
  * and per 128-dim half, by the V rule (z = fp16(min), s = fp16((max - min)/3), k^ = z + c s):
  * the K block holds 64 code rows + 64 meta rows like a V block, and there is no page close.
  * This is the per-token axis that "Half the Cache, Twice the Context" ("What the cache loses
  * when you round it") weighs against per-channel K.  The ring still keeps the last 64 keys
  * exact; a key is read from it only inside the window (t >= seq_len - window), so with window 0
- * every key, the open page's included, comes from its codes.  All calls take it; prefill runs
- * on the CUDA-core split kernel. */
+ * every key, the open page's included, comes from its codes.  All calls take it. */
 /* KVQ_FMT_FP8: K and V rows as OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
  * bits, largest finite 448, no infinity), one byte per value: a (layer, head, K or V) block of a
  * page is 64 rows x 256 B = 16,384 B, half of BF16 -- the FP8 cache of the vLLM study quoted in

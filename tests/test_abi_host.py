@@ -159,7 +159,7 @@ def test_strerror(L):
 def test_format_variants_host_validation(L):
     """Host-side answers for the format variants, all returned before any launch: the 2-bit
     variants need the ring, FP8 does not; a bad FP8 scale is refused by every call; the rotated
-    format refuses prefill."""
+    format's prefill needs no more workspace than the plain format's."""
     tok = kvq.geom(kvq.FMT_HQ2B_TOK, 2, 1, 4)
     had = kvq.geom(kvq.FMT_HQ2B_HAD, 2, 1, 4)
     assert _decode(L, tok, ring=None) == kvq.ERR_INVALID_ARG
@@ -172,9 +172,11 @@ def test_format_variants_host_validation(L):
     assert _decode(L, bad, ring=None) == kvq.ERR_INVALID_ARG
     assert L.kv_quant_append(ctypes.byref(bad), 0, 256, 1 << 24, None, 768, 4, 1, 1024, 1040, 1056, 1, 1,
                              1280, 1536, 2048, None) == kvq.ERR_INVALID_ARG
+    plain = kvq.prefill_workspace_bytes(kvq.geom(kvq.FMT_HQ2B, 2, 1, 4), 16, 256)
+    assert kvq.prefill_workspace_bytes(had, 16, 256) == plain
     rc = L.paged_prefill_attn(ctypes.byref(had), 0, 256, 1 << 22, 512, 0, 768, 4, 1, 1024, 1040, 1056, 16, 16,
-                              1072, 256, 1280, 0.0625, 1536, 1 << 24, 1792, 2048, None)
-    assert rc == kvq.ERR_UNSUPPORTED
+                              1072, 256, 1280, 0.0625, 1536, plain - 256, 1792, 2048, None)
+    assert rc == kvq.ERR_WORKSPACE_TOO_SMALL
 
 
 def _noalloc(L, g, **kw):

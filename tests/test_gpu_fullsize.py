@@ -187,6 +187,34 @@ def test_chunked_prefill_65536_plus_1024_sampled():
         assert np.all(np.isfinite(got))
 
 
+@pytest.mark.parametrize("fmt", [oracle.FMT_HQ2B_TOK, oracle.FMT_HQ2B_HAD, oracle.FMT_FP8])
+def test_chunked_prefill_65536_plus_1024_format_variants_sampled(fmt):
+    """The 1,024-token chunk over the 65,536-token prefix (one layer) in the per-token-K, rotated
+    and FP8 formats on the tensor-core prefill: the first and last rows, the rows at both sides
+    of every fourth CTA tile boundary, and a seeded sample, against the oracle."""
+    wl = synth.chunked_prefill_27b(layers=1)
+    dw = _dw(wl, fmt, fill=None)
+    prefix, chunk = 65536, 1024
+    rows = _prefill_rows(chunk, wl.group, extra=8)[::2]
+    if fmt == oracle.FMT_HQ2B_HAD:
+        # the oracle's rotated format applies a dense 256 x 256 Hadamard matrix to every key of
+        # every query: three rows (first, middle, last) keep it to about a minute
+        rows = [0, 777, chunk - 1]
+    dw.fill_history([prefix])
+    ws, out = dw.prefill_buffers(chunk)
+    k = wl.kv_torch(0, 0, prefix, chunk, 0, "cuda")
+    v = wl.kv_torch(0, 0, prefix, chunk, 1, "cuda")
+    dw.append(0, [0], [prefix], [chunk], k, v)
+    ws.view(torch.int32).fill_(-1)
+    dw.prefill(0, wl.q_torch(0, 0, prefix, chunk, "cuda"), [prefix], [chunk], [0], ws, out)
+    got = out.cpu().numpy()
+    assert dw.cache.read_status() == 0
+    oc = LaneCache(wl, fmt, 0, 0)
+    ref = oc.attend(wl.q_np(0, 0, prefix, chunk)[rows], [prefix + i for i in rows], 0, dw.sm_scale)
+    assert_close(got[rows], ref, what=f"prefill fmt={fmt}")
+    assert np.all(np.isfinite(got))
+
+
 def test_prefill_prefix_over_three_splits_in_full():
     """A 200-token chunk over a 20,000-token prefix: the keys span three 8,192-key splits, so
     every query's result is a merge of three or more split partials; every row and head against

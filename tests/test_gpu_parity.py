@@ -182,16 +182,6 @@ def test_fp8_decode_with_scales(scales):
     assert dw.cache.read_status() == 0
 
 
-def test_rotated_format_refuses_prefill():
-    from compressed_paged_kv_quant_gb300 import kvq
-    wl = _custom([128], L=1, H=1, Hq=4)
-    dw = _dw(wl, HAD)
-    ws, out = dw.prefill_buffers(1)
-    with pytest.raises(kvq.KvqError) as e:
-        dw.prefill(0, dw.step_q(0), [127], [1], [0], ws, out)
-    assert e.value.code == kvq.ERR_UNSUPPORTED
-
-
 def test_bf16_append_bytes():
     wl = _custom([200, 64, 1], L=2, H=2, Hq=4)
     dw = _dw(wl, BF)
@@ -254,19 +244,29 @@ def test_decode_zero_length_lane_gives_zeros():
     assert torch.all(torch.isfinite(out))
 
 
-@pytest.mark.parametrize("fmt,window", [(HQ, 0), (HQ, 64), (BF, 0), (TOK, 0), (TOK, 64), (FP8, 0)])
-def test_prefill_chunks(fmt, window):
-    """Causal chunks over a compressed prefix: (prefix, chunk) = (300, 100), (0, 70), (1000, 1100)."""
+@pytest.mark.parametrize("fmt,window,scales", [(HQ, 0, None), (HQ, 64, None), (BF, 0, None), (TOK, 0, None),
+                                               (TOK, 64, None), (HAD, 0, None), (HAD, 64, None),
+                                               (FP8, 0, None), (FP8, 0, (0.25, 3.0))])
+def test_prefill_chunks(fmt, window, scales):
+    """Causal chunks over a compressed prefix: (prefix, chunk) = (300, 100), (0, 70), (1000, 1100);
+    every compressed format on the tensor-core prefill, BF16 on the CUDA-core split kernel."""
+    scales = scales or (0.0, 0.0)
     prefix, chunk = [300, 0, 1000], [100, 70, 1100]
+    layers = range(2)
+    if fmt == HAD:
+        # the oracle turns every key and value of every query back with a dense 256 x 256
+        # Hadamard matrix: smaller chunks on one layer keep it to seconds
+        prefix, chunk = [128, 0, 260], [40, 24, 72]
+        layers = [1]
     lens = [p + c for p, c in zip(prefix, chunk)]
     wl = _custom(lens, L=2, H=2, Hq=12, window=window)
-    dw = _dw(wl, fmt)
+    dw = _dw(wl, fmt, scales=scales)
     _gpu_fill(dw)            # prefix and chunk K/V appended (the chunk's own K/V first, as required)
-    g, pool, ring = _oracle_full(wl, fmt)
+    g, pool, ring = _oracle_full(wl, fmt, scales=scales)
     rows = sum(chunk)
     ws, out = dw.prefill_buffers(rows)
     offs = np.cumsum([0] + chunk[:-1]).tolist()
-    for layer in range(2):
+    for layer in layers:
         ws.view(torch.int32).fill_(-1)
         q = torch.cat([wl.q_torch(layer, b, prefix[b], chunk[b], "cuda") for b in range(3)])
         dw.prefill(layer, q, prefix, chunk, offs, ws, out)
