@@ -6,11 +6,12 @@
 // decode reads 7.1x the bytes of the 2-bit format and little arithmetic per byte, so this kernel
 // only has to stream pages at HBM rate.
 //
-// CTA = 4 warps = one (lane, KV head, split of DECODE_SPLIT_BF16 tokens), one CTA per SM.  A
-// page's K and V blocks of this layer and head (32 KB each, adjacent in the page) are copied by
-// all 128 threads with 16 B cp.async into a B16_STAGES-deep ring of whole pages whose rows are
-// padded from 512 to 528 B; completion is an mbarrier of 128 cp.async arrivals, every wait
-// bounded.  Warp w takes tokens 16w .. 16w + 15 of every page and runs its own online softmax:
+// CTA = 2 warps = one (lane, KV head, split of DECODE_SPLIT_BF16 tokens), two CTAs per SM, so
+// one CTA's first copies overlap the other's steady stream.  A half page -- the K and V rows of
+// 32 tokens of this layer and head -- is one stage: copied by the 64 threads with 16 B cp.async
+// into a B16_STAGES-deep ring whose rows are padded from 512 to 528 B; completion is an mbarrier
+// of 64 cp.async arrivals, every wait bounded.  Warp w takes tokens 16w .. 16w + 15 of every
+// half page and runs its own online softmax:
 //   S = K . q^T on mma.sync m16n8k16 with bf16 operands as they are stored: A = K rows, B = q of
 //     the group's heads (padded to 8).  Thread column cq reads 16 contiguous bytes (the dims of
 //     two k-steps) of its key rows, so the contraction order over the 256 dims is permuted; a dot
@@ -20,7 +21,7 @@
 //     A: together ~16 significant bits of every weight, so bf16 operands cost no accuracy
 //     against the FP32 oracle.  Thread row g owns 32 contiguous dims of every value row, read in
 //     four 16 B chunks whose order rotates with g so that a warp's reads spread over all banks.
-// At the end the 4 warps' (m, l, O) merge in FP32 in shared memory into one partial record of
+// At the end the 2 warps' (m, l, O) merge in FP32 in shared memory into one partial record of
 // the split; attn_combine merges the splits -- the two-level accumulation of "Half the Cache,
 // Twice the Context", "The cliff is in the accumulator".
 #include "kvq_internal.cuh"
@@ -29,10 +30,11 @@
 
 namespace kvq {
 
-constexpr int B16_WARPS = 4;
-constexpr int B16_STAGES = 3;                                 // whole pages in the ring
+constexpr int B16_WARPS = 2;
+constexpr int B16_STAGES = 3;                                 // half pages in the ring
+constexpr int B16_T = 16 * B16_WARPS;                         // tokens a stage: 32
 constexpr int B16_ROW = 2 * D + 16;                           // a padded 512 B row: 528 B
-constexpr int B16_STAGE_BYTES = 2 * P * B16_ROW;              // K rows then V rows: 67,584 B
+constexpr int B16_STAGE_BYTES = 2 * B16_T * B16_ROW;          // K rows then V rows: 33,792 B
 constexpr int B16_Q_OFF = B16_STAGES * B16_STAGE_BYTES;       // q as B fragments: [8][32 lanes] uint4
 constexpr int B16_BAR_OFF = B16_Q_OFF + 8 * 32 * 16;          // full[S]
 constexpr int B16_SMEM = B16_BAR_OFF + B16_STAGES * 8;
@@ -59,8 +61,8 @@ __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
 // the 16 B chunk of thread row g's j-th read in a value row (its 32 dims are chunks 4g .. 4g+3)
 __device__ __forceinline__ int b16_vchunk(int g, int j) { return 4 * g + ((j + (g >> 1)) & 3); }
 
-// grid (lanes * H, splits); 128 threads
-__global__ void __launch_bounds__(B16_WARPS * 32, 1) decode_bf16_split(AttnArgs a) {
+// grid (lanes * H, splits); 64 threads
+__global__ void __launch_bounds__(B16_WARPS * 32, 2) decode_bf16_split(AttnArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
@@ -74,7 +76,8 @@ __global__ void __launch_bounds__(B16_WARPS * 32, 1) decode_bf16_split(AttnArgs 
   const int t0 = s * a.split_tokens;
   if (t0 >= len) return;                      // the combine reads no record of this split
   const int t1 = min(t0 + a.split_tokens, len);
-  const int p0 = t0 / P, np = (t1 - t0 + P - 1) / P;
+  // stages: half pages of the split (a split starts on a page boundary)
+  const int p0 = t0 / P, np = (t1 - t0 + B16_T - 1) / B16_T;
 
   uint8_t* stage = smem;
   uint4* qf = reinterpret_cast<uint4*>(smem + B16_Q_OFF);
@@ -97,21 +100,25 @@ __global__ void __launch_bounds__(B16_WARPS * 32, 1) decode_bf16_split(AttnArgs 
   }
   __syncthreads();
 
-  // page j of the split into stage j % B16_STAGES, by every thread: 16 B chunk q = thread + 128 i
-  // of the page's 4,096 (K block then V block) to row q / 32, column q % 32 of the padded ring
+  // half page j of the split (tokens 32 (j % 2) .. + 31 of page p0 + j / 2) into stage
+  // j % B16_STAGES, by every thread: 16 B chunk q = thread + 64 i of its 2,048 (K rows then V
+  // rows) to row q / 32, column q % 32 of the padded ring
   uint32_t valid = 0;   // bit per stage: the page is in the pool (same in every thread)
   auto issue = [&](int j) {
     const int st = j % B16_STAGES;
-    const int32_t phys = c.page_table[(int64_t)b * c.max_pages + p0 + j];
+    const int32_t phys = c.page_table[(int64_t)b * c.max_pages + p0 + j / 2];
     const bool ok = phys >= 0 && phys < c.pool_pages;
     valid = ok ? (valid | (1u << st)) : (valid & ~(1u << st));
     if (ok) {
-      const uint8_t* src = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_BF16, H, c.layer, h, 0);
+      const uint8_t* kbl = c.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_BF16, H, c.layer, h, 0) +
+                           (j & 1) * (B16_T * 2 * D);
       const uint32_t dst = smem_u32(stage + st * B16_STAGE_BYTES);
 #pragma unroll 8
-      for (int i = 0; i < 2 * BF16_BLOCK / 16 / (B16_WARPS * 32); i++) {
+      for (int i = 0; i < 2 * B16_T * 2 * D / 16 / (B16_WARPS * 32); i++) {
         const int q = threadIdx.x + B16_WARPS * 32 * i;
-        b16_cp_async16(dst + (q >> 5) * B16_ROW + 16 * (q & 31), src + 16 * q);
+        const int row = q >> 5;   // 0 .. 63: K rows then V rows of the half page
+        const uint8_t* src = kbl + (row >= B16_T ? BF16_BLOCK - B16_T * 2 * D : 0) + 16 * q;
+        b16_cp_async16(dst + row * B16_ROW + 16 * (q & 31), src);
       }
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(FULL(st)) : "memory");
     } else {
@@ -139,7 +146,7 @@ __global__ void __launch_bounds__(B16_WARPS * 32, 1) decode_bf16_split(AttnArgs 
     }
     if (valid & (1u << st)) {
       const uint8_t* kb = stage + st * B16_STAGE_BYTES;
-      const uint8_t* vb = kb + P * B16_ROW;
+      const uint8_t* vb = kb + B16_T * B16_ROW;
       // ---- S = K . q^T for tokens 16 warp + g (+8); k-steps 2p, 2p+1 of thread column cq
       // cover dims 32p + 8cq .. +3 and +4 .. +7 (A regs 0/2: row g, 1/3: row g + 8)
       const uint8_t* krA = kb + (16 * warp + g) * B16_ROW + 16 * cq;
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(B16_WARPS * 32, 1) decode_bf16_split(AttnArgs 
         mma16816_bf16(S, ka.z, kbw.z, ka.w, kbw.w, qw.z, qw.w);
       }
       // scores (log2 domain), keys past the lane's length masked
-      const int tok = (p0 + j) * P + 16 * warp + g;
+      const int tok = p0 * P + j * B16_T + 16 * warp + g;
 #pragma unroll
       for (int e = 0; e < 4; e++) S[e] = (tok + 8 * (e >> 1) < len) ? S[e] * kscale : -INFINITY;
       // ---- online softmax over the warp's 16 tokens, per head
@@ -223,15 +230,15 @@ __global__ void __launch_bounds__(B16_WARPS * 32, 1) decode_bf16_split(AttnArgs 
   __syncthreads();
   if (timed_out) return;   // (uniform) the status word reports it; no partial is written
 
-  // ---- merge the 4 warps: per head the largest m, weights 2^(m_w - m), O and l summed in FP32
+  // ---- merge the warps: per head the largest m, weights 2^(m_w - m), O and l summed in FP32
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, o);
     l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, o);
   }
-  float* sm_m = reinterpret_cast<float*>(smem);                 // [4][8]
-  float* sm_l = sm_m + B16_WARPS * MAX_GROUP;                   // [4][8]
-  float* sm_o = sm_l + B16_WARPS * MAX_GROUP;                   // [4][8 heads][256 dims]
+  float* sm_m = reinterpret_cast<float*>(smem);                 // [warps][8]
+  float* sm_l = sm_m + B16_WARPS * MAX_GROUP;                   // [warps][8]
+  float* sm_o = sm_l + B16_WARPS * MAX_GROUP;                   // [warps][8 heads][256 dims]
   if (g == 0) {
     sm_m[warp * MAX_GROUP + 2 * cq] = m0;
     sm_m[warp * MAX_GROUP + 2 * cq + 1] = m1;
