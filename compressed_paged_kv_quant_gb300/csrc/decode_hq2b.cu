@@ -971,19 +971,29 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
     }
   }
   __syncthreads();
-  // partial k goes to thread group k % 4; each thread sums 4 dims of its group's partials
+  // partial k goes to thread group k % 4; each thread sums 4 dims of its group's partials, eight
+  // partials' loads in flight before any is used (the partials were written by the main grid
+  // moments ago and sit in L2: the merge is latency-bound)
   {
     const int dq = tid & 63, kg = tid >> 6;
     const float4* part = reinterpret_cast<const float4*>(a.ws_o + pbase * D) + dq;
     float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int k = kg; k < nk; k += 4) {
-      const float4 v = part[(int64_t)k * (D / 4)];
-      const float w = s_w[k];
-      s4.x = fmaf(v.x, w, s4.x);
-      s4.y = fmaf(v.y, w, s4.y);
-      s4.z = fmaf(v.z, w, s4.z);
-      s4.w = fmaf(v.w, w, s4.w);
+    for (int k0 = kg; k0 < nk; k0 += 32) {
+      float4 v[8];
+      float w[8];
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        const int k = k0 + 4 * u;
+        v[u] = k < nk ? part[(int64_t)k * (D / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[u] = k < nk ? s_w[k] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; u++) {
+        s4.x = fmaf(v[u].x, w[u], s4.x);
+        s4.y = fmaf(v[u].y, w[u], s4.y);
+        s4.z = fmaf(v[u].z, w[u], s4.z);
+        s4.w = fmaf(v[u].w, w[u], s4.w);
+      }
     }
     reinterpret_cast<float4*>(s_red[kg])[dq] = s4;
   }
