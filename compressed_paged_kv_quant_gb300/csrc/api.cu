@@ -12,6 +12,9 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
 struct AttnArgs;
 int launch_attn_generic(int fmt, const AttnArgs& a, int decode, cudaStream_t stream);
 int launch_decode_hq2b(const AttnArgs& a, cudaStream_t stream);
+int launch_append_last(const CacheView& c, uint8_t* pool, __nv_bfloat16* ring, const int32_t* start_pos,
+                       const int32_t* n_new, const int32_t* tok_offset, int n_rows, int lanes,
+                       const __nv_bfloat16* k, const __nv_bfloat16* v, cudaStream_t stream);
 int launch_decode_fp8(const AttnArgs& a, cudaStream_t stream);
 int launch_decode_bf16(const AttnArgs& a, cudaStream_t stream);
 int decode_split_tokens(int fmt);
@@ -190,21 +193,32 @@ const char* kvq_strerror(int code) {
 
 int kvq_build_arch(void) { return KVQ_SM; }
 
-int kv_quant_append(const kvq_geom* g, int layer, void* pool, size_t pool_bytes, void* ring,
-                    const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
-                    const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows, const void* k,
-                    const void* v, int32_t* d_status, kvq_stream_t stream) {
+// host checks of kv_quant_append; 1 = valid but nothing to do
+static int check_append(const kvq_geom* g, int layer, const void* pool, size_t pool_bytes, const void* ring,
+                        const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
+                        const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows, const void* k,
+                        const void* v, const int32_t* d_status) {
   int rc = check_geom(g);
   if (rc) return rc;
   if (layer < 0 || layer >= g->num_layers || lanes < 0 || max_new < 0 || n_rows < 0 || max_pages < 0)
     return KVQ_ERR_INVALID_ARG;
   if ((int64_t)max_pages * P > (int64_t)INT32_MAX) return KVQ_ERR_INVALID_ARG;
-  if (lanes == 0 || max_new == 0) return KVQ_OK;
+  if (lanes == 0 || max_new == 0) return 1;
   if (!pool || !page_table || !start_pos || !n_new || !tok_offset || !k || !v || !d_status)
     return KVQ_ERR_INVALID_ARG;
   if (two_bit(g->format) && !ring) return KVQ_ERR_INVALID_ARG;
   if (pool_bytes < page_bytes_of(g)) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(pool) || !aligned16(ring) || !aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
+  return KVQ_OK;
+}
+
+int kv_quant_append(const kvq_geom* g, int layer, void* pool, size_t pool_bytes, void* ring,
+                    const int32_t* page_table, int max_pages, int lanes, const int32_t* start_pos,
+                    const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows, const void* k,
+                    const void* v, int32_t* d_status, kvq_stream_t stream) {
+  const int rc = check_append(g, layer, pool, pool_bytes, ring, page_table, max_pages, lanes, start_pos, n_new,
+                              tok_offset, max_new, n_rows, k, v, d_status);
+  if (rc) return rc == 1 ? KVQ_OK : rc;
   CacheView c = make_view(g, layer, pool, pool_bytes, ring, page_table, max_pages, 0, d_status);
   return launch_append(layout_fmt(g->format), c, static_cast<uint8_t*>(pool), static_cast<__nv_bfloat16*>(ring), start_pos,
                        n_new, tok_offset, max_new, n_rows, lanes, static_cast<const __nv_bfloat16*>(k),
@@ -284,11 +298,21 @@ int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes,
   if (!start_pos || !n_new || !tok_offset || !k || !v) return KVQ_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(v)) return KVQ_ERR_ALIGNMENT;
   if (ws_bytes < kvq_decode_workspace_bytes(g, lanes, max_seq_len)) return KVQ_ERR_WORKSPACE_TOO_SMALL;
-  // the append first: a one-launch decode append (at most one token per lane)
-  rc = kv_quant_append(g, layer, pool, pool_bytes, ring, page_table, max_pages, lanes, start_pos, n_new, tok_offset,
-                       1, n_rows, k, v, d_status, stream);
-  if (rc) return rc;
-  if (g->format != KVQ_FMT_HQ2B || lanes > 8192)   // BF16 or rotated pages, very many lanes: plain decode
+  rc = check_append(g, layer, pool, pool_bytes, ring, page_table, max_pages, lanes, start_pos, n_new, tok_offset, 1,
+                    n_rows, k, v, d_status);
+  if (rc < 0) return rc;
+  const bool fused = g->format == KVQ_FMT_HQ2B && lanes <= 8192;
+  // With a window of a whole page nothing this step's attention reads is written by its append:
+  // the main pages end before the window, the tail takes its keys from the ring slots the append
+  // leaves alone and the step's own token from `k` / `v`.  The append then runs last, overlapping
+  // the combine.  Otherwise it runs first (a one-launch decode append, at most one token a lane).
+  const bool append_last = fused && window == P;
+  if (!append_last) {
+    rc = kv_quant_append(g, layer, pool, pool_bytes, ring, page_table, max_pages, lanes, start_pos, n_new,
+                         tok_offset, 1, n_rows, k, v, d_status, stream);
+    if (rc) return rc;
+  }
+  if (!fused)   // BF16, FP8, per-token-K or rotated pages, very many lanes: plain decode
     return paged_decode_attn(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
                              max_seq_len, q, sm_scale, workspace, ws_bytes, out, d_status, stream);
   AttnArgs a = decode_args(g, layer, pool, pool_bytes, ring, window, page_table, max_pages, lanes, seq_len,
@@ -300,7 +324,12 @@ int kvq_decode_step(const kvq_geom* g, int layer, void* pool, size_t pool_bytes,
   a.step.k = static_cast<const __nv_bfloat16*>(k);
   a.step.v = static_cast<const __nv_bfloat16*>(v);
   a.step.active = 1;
-  return launch_decode_hq2b(a, (cudaStream_t)stream);
+  a.step.append_last = append_last ? 1 : 0;
+  rc = launch_decode_hq2b(a, (cudaStream_t)stream);
+  if (rc || !append_last) return rc;
+  return launch_append_last(a.c, static_cast<uint8_t*>(pool), static_cast<__nv_bfloat16*>(ring), start_pos, n_new,
+                            tok_offset, n_rows, lanes, static_cast<const __nv_bfloat16*>(k),
+                            static_cast<const __nv_bfloat16*>(v), (cudaStream_t)stream);
 }
 
 static int page_move(const kvq_geom* g, void* pool, size_t pool_bytes, const int32_t* page_ids, int n_pages,

@@ -53,11 +53,11 @@ __global__ void __launch_bounds__(256) append_rows_kernel(AppendArgs a) {
 // KGROUP_THREADS, 4 groups), or one 1,024-thread CTA the whole block (the rotated format, whose
 // keys are rotated a row at a time).  The page close reads ring slots 0..62 and this token's key
 // from `k`; the row write touches slot 63 only, so the two never meet.
+// LAST: launched as the programmatic dependent of the decode step's combine kernel (nothing the
+// step's attention reads is written here); every CTA waits for that grid before it exits, so the
+// kernel after this one in the stream sees the whole step complete.
 template <int FMT, int THREADS>
-__global__ void __launch_bounds__(THREADS) append_one_kernel(AppendArgs a) {
-  // a decode kernel launched as this grid's programmatic dependent (kvq_decode_step) may start
-  // now; it waits for this grid before it reads anything written here
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+__device__ __forceinline__ void append_one(const AppendArgs& a) {
   const int b = blockIdx.x, h = blockIdx.y, grp = blockIdx.z;
   int start, n, off;
   if (!read_lane(a, b, start, n, off) || n == 0) return;
@@ -68,6 +68,35 @@ __global__ void __launch_bounds__(THREADS) append_one_kernel(AppendArgs a) {
   }
 }
 
+template <int FMT, int THREADS, bool LAST>
+__global__ void __launch_bounds__(THREADS) append_one_kernel(AppendArgs a) {
+  // a decode kernel launched as this grid's programmatic dependent (kvq_decode_step) may start
+  // now; it waits for this grid before it reads anything written here
+  if (!LAST) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  append_one<FMT, THREADS>(a);
+  if (LAST) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+// Decode-step append of the plain 2-bit format as the programmatic dependent of the kernel just
+// launched on `stream` (see append_one_kernel's LAST).
+int launch_append_last(const CacheView& c, uint8_t* pool, __nv_bfloat16* ring, const int32_t* start_pos,
+                       const int32_t* n_new, const int32_t* tok_offset, int n_rows, int lanes,
+                       const __nv_bfloat16* k, const __nv_bfloat16* v, cudaStream_t stream) {
+  AppendArgs a{c, pool, ring, start_pos, n_new, tok_offset, 1, n_rows, lanes, k, v};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(lanes, c.num_kv_heads, D / KGROUP_CH);
+  cfg.blockDim = dim3(KGROUP_THREADS);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, append_one_kernel<KVQ_FMT_HQ2B, KGROUP_THREADS, true>, a) != cudaSuccess)
+    return KVQ_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* ring, const int32_t* start_pos,
                   const int32_t* n_new, const int32_t* tok_offset, int max_new, int n_rows, int lanes,
                   const __nv_bfloat16* k, const __nv_bfloat16* v, cudaStream_t stream) {
@@ -75,14 +104,14 @@ int launch_append(int fmt, const CacheView& c, uint8_t* pool, __nv_bfloat16* rin
   if (max_new == 1) {
     dim3 g1(lanes, c.num_kv_heads);
     if (fmt == KVQ_FMT_HQ2B && c.rotated) {
-      append_one_kernel<KVQ_FMT_HQ2B, KCLOSE_THREADS><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
+      append_one_kernel<KVQ_FMT_HQ2B, KCLOSE_THREADS, false><<<g1, KCLOSE_THREADS, 0, stream>>>(a);
     } else if (fmt == KVQ_FMT_HQ2B) {
       const dim3 gg(lanes, c.num_kv_heads, c.ktok ? 1 : D / KGROUP_CH);
-      append_one_kernel<KVQ_FMT_HQ2B, KGROUP_THREADS><<<gg, KGROUP_THREADS, 0, stream>>>(a);
+      append_one_kernel<KVQ_FMT_HQ2B, KGROUP_THREADS, false><<<gg, KGROUP_THREADS, 0, stream>>>(a);
     } else if (fmt == KVQ_FMT_FP8) {
-      append_one_kernel<KVQ_FMT_FP8, KGROUP_THREADS><<<g1, KGROUP_THREADS, 0, stream>>>(a);
+      append_one_kernel<KVQ_FMT_FP8, KGROUP_THREADS, false><<<g1, KGROUP_THREADS, 0, stream>>>(a);
     } else {
-      append_one_kernel<KVQ_FMT_BF16, KGROUP_THREADS><<<g1, KGROUP_THREADS, 0, stream>>>(a);
+      append_one_kernel<KVQ_FMT_BF16, KGROUP_THREADS, false><<<g1, KGROUP_THREADS, 0, stream>>>(a);
     }
   } else if (fmt == KVQ_FMT_HQ2B) {
     if (!c.ktok) {   // the per-token-K format has no page close

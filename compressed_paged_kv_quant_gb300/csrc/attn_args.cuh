@@ -14,6 +14,9 @@ struct StepAppend {
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
   int active;
+  // 1: nothing this step reads is written by its append (window == 64), so the append runs last,
+  // as the programmatic dependent of the combine kernel, instead of first
+  int append_last;
 };
 
 struct AttnArgs {

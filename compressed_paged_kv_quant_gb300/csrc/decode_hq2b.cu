@@ -688,6 +688,9 @@ __global__ void __launch_bounds__(DEC_PAIRS * 64, DEC_CTAS_PER_SM) decode_hq2b_m
 constexpr int TAIL_MAX = 2 * P;   // len - tail_start < 2 pages, since the window is at most a page
 
 __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
+  // fused decode step whose append runs last: that kernel may be scheduled now (it touches
+  // nothing this kernel reads, and waits for this grid before it exits)
+  if (a.step.append_last) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
   const CacheView& c = a.c;
   const int H = c.num_kv_heads, G = c.group, Hq = c.num_q_heads;
   const int b = blockIdx.x, j = blockIdx.y, h = j / G;
@@ -936,6 +939,19 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
     nk = (segstart + npg - 1) / Wp - segstart / Wp + 1;
   }
   const int64_t pbase = ((int64_t)b * Hq + j) * a.max_splits;
+  // partial k goes to thread group k % 4; each thread sums 4 dims of its group's partials.  The
+  // partials were written by the main grid moments ago and sit in L2, so the merge is
+  // latency-bound: the loads of the first COMB_PRE partials of every group go out before warp 0
+  // reads the (m, l) pairs, and the weights meet them after one round trip
+  constexpr int COMB_PRE = 12;
+  const int dq = tid & 63, kg = tid >> 6;
+  const float4* part = reinterpret_cast<const float4*>(a.ws_o + pbase * D) + dq;
+  float4 v0[COMB_PRE];
+#pragma unroll
+  for (int u = 0; u < COMB_PRE; u++) {
+    const int k = kg + 4 * u;
+    v0[u] = k < nk ? part[(int64_t)k * (D / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (warp == 0) {
     const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + pbase;
     float mk[DEC_MAX_SLOTS / 32], lk[DEC_MAX_SLOTS / 32];
@@ -971,14 +987,18 @@ __global__ void __launch_bounds__(256, 1) decode_hq2b_combine(AttnArgs a) {
     }
   }
   __syncthreads();
-  // partial k goes to thread group k % 4; each thread sums 4 dims of its group's partials, eight
-  // partials' loads in flight before any is used (the partials were written by the main grid
-  // moments ago and sit in L2: the merge is latency-bound)
   {
-    const int dq = tid & 63, kg = tid >> 6;
-    const float4* part = reinterpret_cast<const float4*>(a.ws_o + pbase * D) + dq;
     float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k0 = kg; k0 < nk; k0 += 32) {
+#pragma unroll
+    for (int u = 0; u < COMB_PRE; u++) {
+      const int k = kg + 4 * u;
+      const float w = k < nk ? s_w[k] : 0.f;
+      s4.x = fmaf(v0[u].x, w, s4.x);
+      s4.y = fmaf(v0[u].y, w, s4.y);
+      s4.z = fmaf(v0[u].z, w, s4.z);
+      s4.w = fmaf(v0[u].w, w, s4.w);
+    }
+    for (int k0 = kg + 4 * COMB_PRE; k0 < nk; k0 += 32) {   // the rest, eight loads in flight at a time
       float4 v[8];
       float w[8];
 #pragma unroll
@@ -1103,7 +1123,7 @@ int launch_decode_hq2b(const AttnArgs& a_in, cudaStream_t stream) {
     const int rows = a.lanes * a.c.num_q_heads;
     rotate_q_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(a);
   }
-  if (a.step.active) {
+  if (a.step.active && !a.step.append_last) {
     // fused decode step: overlap the append kernel launched just before
     cudaLaunchConfig_t mc = {};
     mc.gridDim = dim3(grid);

@@ -10,6 +10,7 @@
 //
 // Grid: (chunks of 16 KB per page, pages); 256 threads; each thread moves 4 x 16 B per chunk.
 #include "kvq_internal.cuh"
+#include "mma_tma.cuh"
 
 namespace kvq {
 
@@ -56,3 +57,26 @@ int launch_page_move(uint8_t* pool, uint8_t* arena, const int32_t* page_ids, int
 }
 
 }  // namespace kvq
+
+// ----------------------------------------------------------------------------- failure path
+namespace kvq {
+// One warp waits, with the bounded wait every kernel of the library uses, on an mbarrier that
+// nothing arrives at: the wait gives up after its iteration limit (tens of milliseconds), the
+// kernel sets KVQ_STATUS_TIMEOUT and returns, and the context stays usable.
+__global__ void wait_timeout_kernel(int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(&bar)), "r"(1u) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  const bool done = __all_sync(0xFFFFFFFFu, mbar_wait(smem_u32(&bar), 0u));
+  if (!done && threadIdx.x == 0) flag(status, KVQ_STATUS_TIMEOUT);
+}
+}  // namespace kvq
+
+extern "C" int kvq_selftest_wait_timeout(int32_t* d_status, kvq_stream_t stream) {
+  if (!d_status) return KVQ_ERR_INVALID_ARG;
+  kvq::wait_timeout_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(d_status);
+  return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}

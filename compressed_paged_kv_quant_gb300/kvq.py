@@ -38,7 +38,8 @@ STATUS_TIMEOUT = 16
 EXPORTS = ("kvq_page_bytes", "kvq_token_bytes", "kvq_ring_bytes", "kvq_pool_pages",
            "kvq_decode_workspace_bytes", "kvq_prefill_workspace_bytes", "kvq_strerror",
            "kvq_build_arch", "kv_quant_append", "paged_decode_attn", "paged_prefill_attn",
-           "paged_decode_attn_noalloc", "kvq_decode_step", "kvq_pages_gather", "kvq_pages_scatter")
+           "paged_decode_attn_noalloc", "kvq_decode_step", "kvq_pages_gather", "kvq_pages_scatter",
+           "kvq_selftest_wait_timeout")
 
 
 class KvqError(RuntimeError):
@@ -112,6 +113,8 @@ def lib():
             L.kvq_pages_gather.restype = i32
             L.kvq_pages_scatter.argtypes = [G, P, sz, P, i32, P, P, P]
             L.kvq_pages_scatter.restype = i32
+            L.kvq_selftest_wait_timeout.argtypes = [P, P]
+            L.kvq_selftest_wait_timeout.restype = i32
             _lib = L
     return _lib
 
@@ -239,6 +242,11 @@ def pages_scatter(g: Geom, pool, page_ids, arena, status, stream=None):
     rc = lib().kvq_pages_scatter(ctypes.byref(g), _ptr(pool), _nbytes(pool), _ptr(page_ids), page_ids.numel(),
                                  _arena_ptr(arena), _ptr(status), _stream(stream))
     _check(rc, "kvq_pages_scatter")
+
+
+def selftest_wait_timeout(status, stream=None):
+    """Run one bounded barrier wait that nothing ends (see ``kvq_selftest_wait_timeout``)."""
+    _check(lib().kvq_selftest_wait_timeout(_ptr(status), _stream(stream)), "kvq_selftest_wait_timeout")
 
 
 def paged_prefill_attn(g: Geom, layer: int, pool, ring, window: int, page_table, q_pos0, n_q,

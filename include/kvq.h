@@ -247,6 +247,19 @@ int kvq_pages_scatter(const kvq_geom* geom, void* pool, size_t pool_bytes, const
                       int n_pages, const void* arena, int32_t* d_status, kvq_stream_t stream);
 
 /*
+ * kvq_selftest_wait_timeout -- the library's failure path, run on purpose.  Not an operation
+ * of the method: it exists so that a caller can check, on a healthy GPU, what every kernel of
+ * the library does when a shared-memory barrier wait runs out.  One warp waits, with the same
+ * bounded wait the attention and append kernels use (2^16 tries of mbarrier.try_wait with a
+ * ~1 us suspend hint each, so tens of milliseconds), on a barrier that nothing ever arrives
+ * at; the wait gives up, the kernel ORs KVQ_STATUS_TIMEOUT into *d_status and returns.
+ * Nothing faults or traps and the context stays usable.
+ *   d_status: device int32, not cleared by the call.  Errors: KVQ_ERR_INVALID_ARG (null
+ *   d_status) / KVQ_ERR_CUDA (launch failed).
+ */
+int kvq_selftest_wait_timeout(int32_t* d_status, kvq_stream_t stream);
+
+/*
  * paged_decode_attn_noalloc -- paged_decode_attn without a caller workspace.  The pages have
  * no counterpart of this call: it exists for callers that cannot allocate device memory --
  * plugins of a serving engine whose allocator owns all of the GPU's memory and hands out no

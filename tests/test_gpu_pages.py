@@ -96,3 +96,28 @@ def test_page_move_flags_bad_id():
     assert dw.cache.read_status() == oracle.PAGE_OOB
     a = arena.cpu().numpy()
     assert np.all(a[:pb] == 0x11) and np.all(a[pb:] == 0x77)     # the bad slot is left alone
+
+
+def test_bounded_wait_runs_out_and_context_stays_usable():
+    """A barrier wait that nothing ends gives up within its bound: the TIMEOUT status bit is set,
+    the call returns, and the context then runs further kernels (the library's own page move)."""
+    import time
+    from compressed_paged_kv_quant_gb300 import kvq
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    kvq.selftest_wait_timeout(status)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(status.item()) == kvq.STATUS_TIMEOUT
+    assert elapsed < 5.0
+    g = kvq.Geom(oracle.FMT_HQ2B, 2, 2, 8, 256, 64, 1.0, 1.0)
+    pb = kvq.page_bytes(g)
+    pool = torch.arange(4 * pb, device="cuda").to(torch.uint8)
+    arena = torch.zeros(2 * pb, dtype=torch.uint8, device="cuda")
+    ids = torch.tensor([3, 1], dtype=torch.int32, device="cuda")
+    st2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kvq.pages_gather(g, pool, ids, arena, st2)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == 0
+    assert torch.equal(arena[:pb], pool[3 * pb:4 * pb]) and torch.equal(arena[pb:], pool[pb:2 * pb])
