@@ -264,8 +264,11 @@ __device__ __forceinline__ void kblock_store(const AppendArgs& a, int b, int h, 
 constexpr int KGROUP_CH = 64;
 constexpr int KGROUP_THREADS = 256;
 __device__ __forceinline__ void kclose_group(const AppendArgs& a, int b, int h, int p, int start, int off, int grp) {
-  if (!kblock_page_ok(a.c, b, p)) return;
   const CacheView& c = a.c;
+  if (p >= c.max_pages) {
+    if (threadIdx.x == 0) flag(c.status, KVQ_STATUS_LEN_GT_TABLE);
+    return;
+  }
   const int H = c.num_kv_heads;
   const int cl = threadIdx.x & (KGROUP_CH - 1), part = threadIdx.x / KGROUP_CH, d = KGROUP_CH * grp + cl;
   constexpr int PARTS = KGROUP_THREADS / KGROUP_CH;
@@ -273,23 +276,38 @@ __device__ __forceinline__ void kclose_group(const AppendArgs& a, int b, int h, 
   __shared__ __align__(16) uint8_t codes[P * (KGROUP_CH / 4)];   // 64 key rows x 16 B
   __shared__ __half scales[KGROUP_CH];
   __shared__ float part_max[PARTS][KGROUP_CH];
-  float x[T];
-  float amax = 0.0f;
-  bool bad = false;
+  // Every load of the close goes out before any is used (one round trip, not three): the page
+  // id, the thread's T keys of channel d, and the first of its share of the input rows' values
+  // for the finite check (every channel of the keys that come from this call's input rows; ring
+  // rows were checked when they were appended: a bad value anywhere in them leaves the whole K
+  // block unwritten, in all four group CTAs alike, as a whole-page close would).
+  const int32_t phys = c.page_table[(int64_t)b * c.max_pages + p];
+  __nv_bfloat16 xr[T];
 #pragma unroll
   for (int i = 0; i < T; i++) {
     const int t = T * part + i;
     const int pos = p * P + t;
-    x[i] = __bfloat162float(pos < start ? a.ring[ring_row_offset(c, b, h, t) + d]
-                                        : a.k[((int64_t)(off + pos - start) * H + h) * D + d]);
+    xr[i] = pos < start ? a.ring[ring_row_offset(c, b, h, t) + d] : a.k[((int64_t)(off + pos - start) * H + h) * D + d];
+  }
+  const int first = max(0, start - p * P), n_in = (P - first) * D;
+  const __nv_bfloat16 in0 = (int)threadIdx.x < n_in
+                                ? a.k[((int64_t)(off + p * P + first + threadIdx.x / D - start) * H + h) * D + threadIdx.x % D]
+                                : __float2bfloat16(0.0f);
+  if (phys < 0 || phys >= c.pool_pages) {
+    if (threadIdx.x == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
+    return;
+  }
+  float x[T];
+  float amax = 0.0f;
+  bool bad = !finite16(__bfloat162float(in0));
+#pragma unroll
+  for (int i = 0; i < T; i++) {
+    x[i] = __bfloat162float(xr[i]);
     bad |= !finite16(x[i]);
     amax = fmaxf(amax, fabsf(x[i]));
   }
   part_max[part][cl] = amax;
-  // every channel of the page's keys that come from this call's input rows (ring rows were
-  // checked when they were appended): a bad value anywhere in them leaves the whole K block
-  // unwritten, in all four group CTAs alike, as a whole-page close would
-  for (int i = threadIdx.x, first = max(0, start - p * P); i < (P - first) * D; i += KGROUP_THREADS) {
+  for (int i = threadIdx.x + KGROUP_THREADS; i < n_in; i += KGROUP_THREADS) {   // more than one input row
     const int pos = p * P + first + i / D;
     bad |= !finite16(__bfloat162float(a.k[((int64_t)(off + pos - start) * H + h) * D + i % D]));
   }
@@ -321,7 +339,6 @@ __device__ __forceinline__ void kclose_group(const AppendArgs& a, int b, int h, 
   if (part == 0) scales[cl] = sh;
   __syncthreads();
   if (threadIdx.x < P) {
-    const int32_t phys = c.page_table[(int64_t)b * c.max_pages + p];
     uint8_t* kblk = a.pool + (int64_t)phys * c.page_bytes + block_offset(KVQ_FMT_HQ2B, H, c.layer, h, 0);
     *reinterpret_cast<uint4*>(kblk + threadIdx.x * HQ2B_ROW + (KGROUP_CH / 4) * grp) =
         reinterpret_cast<const uint4*>(codes)[threadIdx.x];
@@ -359,14 +376,16 @@ __device__ __forceinline__ void append_row(const AppendArgs& a, int b, int h, in
     if (lane == 0) flag(c.status, KVQ_STATUS_LEN_GT_TABLE);
     return;
   }
+  // the page id and the token's rows in one round trip (the rows are inside the inputs whatever
+  // the page id)
   const int32_t phys = c.page_table[(int64_t)b * c.max_pages + t / P];
+  const uint4 kx = reinterpret_cast<const uint4*>(a.k + (row * H + h) * D)[lane];
+  const uint4 vx = reinterpret_cast<const uint4*>(a.v + (row * H + h) * D)[lane];
   if (phys < 0 || phys >= c.pool_pages) {
     if (lane == 0) flag(c.status, KVQ_STATUS_PAGE_OOB);
     return;
   }
   const int slot = (int)(t % P);
-  const uint4 kx = reinterpret_cast<const uint4*>(a.k + (row * H + h) * D)[lane];
-  const uint4 vx = reinterpret_cast<const uint4*>(a.v + (row * H + h) * D)[lane];
   if (__any_sync(0xFFFFFFFFu, !(row8_ok(kx) && row8_ok(vx)))) {
     if (lane == 0) flag(c.status, KVQ_STATUS_BAD_INPUT);
     return;
