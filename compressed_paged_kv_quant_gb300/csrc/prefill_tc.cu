@@ -126,6 +126,13 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory")
 
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+// Registers written by tcgen05.ld hold their values only after tcgen05.wait::ld: after the wait,
+// each passes through an empty volatile asm, so that no read of it is scheduled above the wait.
+template <int N>
+__device__ __forceinline__ void tc_regs_ready(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < N; i++) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
 // shared-memory matrix descriptor: 128B swizzle, K-major, 8-row groups 1,024 B apart
@@ -164,6 +171,32 @@ __device__ __forceinline__ float ex2f(float x) {  // 2^x, one MUFU.EX2
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Blackwell's three-input max and paired FP32 arithmetic (two lanes of one 64-bit register, each
+// an IEEE operation): half the softmax's max, FMA and add instructions
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t p;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(p) : "f"(a), "f"(b));
+  return p;
+}
+__device__ __forceinline__ void f2split(uint64_t p, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(a), "=f"(b) : "l"(p));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 __device__ __forceinline__ uint32_t h2u(__half2 x) { return *reinterpret_cast<uint32_t*>(&x); }
@@ -320,28 +353,33 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
       TC_LD32(tl + TM_S0 + 64 * buf, sv);
       TC_LD32(tl + TM_S0 + 64 * buf + 32, (sv + 32));
       tc_wait_ld();
+      tc_regs_ready<64>(sv);
       const int key0 = (p0 + j) * P;
       // a tile entirely below the causal diagonal of every row of the CTA needs no mask (rows
       // past the last query hold Q = 0 and are never written)
       const bool full = key0 + P - 1 <= qpos0 + q_first;
-      // row max and (below) row sum as 8 independent chains: the softmax sits between S and
-      // P.V on the tensor pipe, so its latency, not its instruction count, is what matters
-      float t8[8];
+      // row max and (below) row sum as independent chains (the softmax sits between S and P.V on
+      // the tensor pipe, so its latency matters), on three-input max and paired FP32 operations
+      // (the warps share their SM sub-partitions' issue slots with the dequantisation)
+      float t4[4];
 #pragma unroll
-      for (int i = 0; i < 8; i++) t8[i] = -INFINITY;
+      for (int i = 0; i < 4; i++) t4[i] = -INFINITY;
       if (full) {
 #pragma unroll
-        for (int cidx = 0; cidx < 64; cidx++) t8[cidx & 7] = fmaxf(t8[cidx & 7], __uint_as_float(sv[cidx]));
+        for (int cidx = 0; cidx < 64; cidx += 2)
+          t4[(cidx >> 1) & 3] = fmax3f(t4[(cidx >> 1) & 3], __uint_as_float(sv[cidx]), __uint_as_float(sv[cidx + 1]));
       } else {
 #pragma unroll
-        for (int cidx = 0; cidx < 64; cidx++) {
-          const bool ok = row_valid && key0 + cidx <= qpos;
-          const float x = ok ? __uint_as_float(sv[cidx]) * sl2 : -INFINITY;
-          sv[cidx] = __float_as_uint(x);
-          t8[cidx & 7] = fmaxf(t8[cidx & 7], x);
+        for (int cidx = 0; cidx < 64; cidx += 2) {
+          const bool ok0 = row_valid && key0 + cidx <= qpos, ok1 = row_valid && key0 + cidx + 1 <= qpos;
+          const float x0 = ok0 ? __uint_as_float(sv[cidx]) * sl2 : -INFINITY;
+          const float x1 = ok1 ? __uint_as_float(sv[cidx + 1]) * sl2 : -INFINITY;
+          sv[cidx] = __float_as_uint(x0);
+          sv[cidx + 1] = __float_as_uint(x1);
+          t4[(cidx >> 1) & 3] = fmax3f(t4[(cidx >> 1) & 3], x0, x1);
         }
       }
-      float tmax = fmaxf(fmaxf(fmaxf(t8[0], t8[1]), fmaxf(t8[2], t8[3])), fmaxf(fmaxf(t8[4], t8[5]), fmaxf(t8[6], t8[7])));
+      float tmax = fmaxf(fmax3f(t4[0], t4[1], t4[2]), t4[3]);
       if (full) tmax *= sl2;
       const float m_new = fmaxf(m_run, tmax);
       const bool first = (j == 0) || (m_run == -INFINITY);
@@ -358,6 +396,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           uint32_t o[32];
           TC_LD32(tl + TM_O + 32 * ch, o);
           tc_wait_ld();
+          tc_regs_ready<32>(o);
 #pragma unroll
           for (int i = 0; i < 32; i++) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           TC_ST32(tl + TM_O + 32 * ch, o);
@@ -371,29 +410,27 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
       if (first) m_run = m_new;
       const float m_use = m_run == -INFINITY ? 0.f : m_run;
       uint32_t pr[32];
-      float ps[8];
+      uint64_t ps2[4];   // row sum: 4 chains of key pairs
 #pragma unroll
-      for (int i = 0; i < 8; i++) ps[i] = 0.f;
-      if (full) {
-        const float sc = sl2, nm = -m_use;
-#pragma unroll
-        for (int i = 0; i < 32; i++) {
-          const float e0 = ex2f(fmaf(__uint_as_float(sv[2 * i]), sc, nm));
-          const float e1 = ex2f(fmaf(__uint_as_float(sv[2 * i + 1]), sc, nm));
-          ps[i & 7] += e0 + e1;
-          pr[i] = h2u(__floats2half2_rn(e0, e1));
-        }
-      } else {
+      for (int i = 0; i < 4; i++) ps2[i] = 0ull;   // (+0, +0)
+      {
+        // 2^(x sc - m) for the pair of keys 2i, 2i + 1; masked keys hold -inf (2^-inf = 0)
+        const uint64_t sc2 = full ? f2(sl2, sl2) : f2(1.0f, 1.0f), nm2 = f2(-m_use, -m_use);
 #pragma unroll
         for (int i = 0; i < 32; i++) {
-          const float x0 = __uint_as_float(sv[2 * i]), x1 = __uint_as_float(sv[2 * i + 1]);
-          const float e0 = ex2f(x0 - m_use);   // 2^-inf = 0 for masked keys
-          const float e1 = ex2f(x1 - m_use);
-          ps[i & 7] += e0 + e1;
+          float a0, a1;
+          f2split(fma_f2(f2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), sc2, nm2), a0, a1);
+          const float e0 = ex2f(a0), e1 = ex2f(a1);
+          ps2[i & 3] = add_f2(ps2[i & 3], f2(e0, e1));
           pr[i] = h2u(__floats2half2_rn(e0, e1));
         }
       }
-      l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      {
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 4; i++) f2split(ps2[i], q[2 * i], q[2 * i + 1]);
+        l_run += ((q[0] + q[1]) + (q[2] + q[3])) + ((q[4] + q[5]) + (q[6] + q[7]));
+      }
       TC_ST32(tl + TM_S0 + 64 * buf, pr);
       tc_wait_st();
       tc_fence_before();
@@ -413,6 +450,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
         uint32_t o[32];
         TC_LD32(tl + TM_O + 32 * ch, o);
         tc_wait_ld();
+        tc_regs_ready<32>(o);
         if (row_valid) {
           float4* dst = reinterpret_cast<float4*>(a.ws_o + pidx * D + 32 * ch);
 #pragma unroll
@@ -530,7 +568,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           lo = make_uint4(l[0], l[1], l[2], l[3]);
         };
         if (LY::KSPLIT && key0 + P <= ef) {
-#pragma unroll 2
+#pragma unroll 4
           for (int t = t0; t < P; t += KSTEP) {
             uint4 hi, lo;
             key_split(t, hi, lo);
@@ -538,10 +576,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
             st_shared_v4(kb + 32768 + swz(t, cc & 7), lo);
           }
         } else if (key0 + P <= ef) {   // every key of the tile comes from the page (ef <= len)
-#pragma unroll 2
+#pragma unroll 4
           for (int t = t0; t < P; t += KSTEP) st_shared_v4(kb + swz(t, cc & 7), key_code(t));
         } else
-#pragma unroll 2
+#pragma unroll 4
         for (int t = t0; t < P; t += KSTEP) {
           const int kp = key0 + t;
           uint4 o = make_uint4(0u, 0u, 0u, 0u), olo = make_uint4(0u, 0u, 0u, 0u);
@@ -571,7 +609,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
       const uint32_t vb = sm_u32(smem + LY::SM_V + buf * LY::V_BUF) + tile_off;
       const uint32_t vst = stg + block_bytes(LY::LFMT);
       const bool vall = key0 + P <= len;
-#pragma unroll 2
+#pragma unroll 4
       for (int t = t0; t < P; t += KSTEP) {
         uint4 o = make_uint4(0u, 0u, 0u, 0u), olo = make_uint4(0u, 0u, 0u, 0u);
         if (vall || key0 + t < len) {
