@@ -46,13 +46,12 @@ template <int FMT>
 struct PfLayout {
   static constexpr int LFMT = FMT == KVQ_FMT_FP8 ? KVQ_FMT_FP8 : KVQ_FMT_HQ2B;   // byte layout
   static constexpr bool KSPLIT = FMT == KVQ_FMT_HQ2B_TOK || FMT == KVQ_FMT_HQ2B_HAD;
-  static constexpr bool VSPLIT = false;
   static constexpr int K_BUF = KSPLIT ? 65536 : 32768;   // one K tile buffer (hi, then lo)
-  static constexpr int V_BUF = VSPLIT ? 65536 : 32768;   // one V tile buffer (hi, then lo)
+  static constexpr int V_BUF = 32768;                     // one V tile buffer
   static constexpr int SM_V = 2 * K_BUF;
   static constexpr int SM_STG = SM_V + 2 * V_BUF;
   static constexpr int STAGE = 2 * block_bytes(LFMT);
-  static constexpr int NSTG = LFMT == KVQ_FMT_FP8 ? 2 : (KSPLIT || VSPLIT) ? 3 : 6;
+  static constexpr int NSTG = LFMT == KVQ_FMT_FP8 ? 2 : KSPLIT ? 3 : 6;
   static constexpr int SM_BAR = SM_STG + NSTG * STAGE;
   static constexpr int NUM_BARS = 13 + 2 * NSTG;
   static constexpr int SM_ABORT = SM_BAR + NUM_BARS * 8;
@@ -500,6 +499,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
     // bytes of swizzled chunks, free of bank conflicts.
     const int cc = tid & 31, t0 = tid >> 5;
     constexpr int KSTEP = DQ_T / 32;
+    constexpr int DQ_MAXI = (P + KSTEP - 1) / KSTEP;   // keys a thread takes of a tile, at most
     const uint32_t tile_off = (uint32_t)(cc >> 3) * 8192u;
     for (int j = 0; j < ntiles && !timed_out; j++) {
       const int buf = j & 1;
@@ -520,16 +520,25 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           const uint4 sc = ld_shared_v4(stg + HQ2B_META_OFF + 16 * cc);
           scs[0] = sc.x; scs[1] = sc.y; scs[2] = sc.z; scs[3] = sc.w;
         }
-        // codes (or E4M3 bytes) of key t, dims 8cc .. 8cc + 7 -> 4 fp16 pairs
-        auto key_code = [&](int t) -> uint4 {
+        // The raw words of key t (dims 8cc .. 8cc + 7): ra, rb = its two code bytes (2-bit
+        // layouts) or its two E4M3 words (FP8); rm = its metadata word (per-token-K format).
+        auto key_raw = [&](int t, uint32_t& ra, uint32_t& rb, uint32_t& rm) {
+          if constexpr (FP8) {
+            ra = ld_shared_u32(stg + t * D + 8 * cc);
+            rb = ld_shared_u32(stg + t * D + 8 * cc + 4);
+          } else {
+            ra = ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc);
+            rb = ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1);
+            if constexpr (FMT == KVQ_FMT_HQ2B_TOK) rm = ld_shared_u32(stg + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+          }
+        };
+        // raw words -> 4 fp16 pairs of k^ (plain 2-bit and FP8 layouts)
+        auto key_code = [&](uint32_t ra, uint32_t rb) -> uint4 {
           uint32_t res[4];
           if constexpr (FP8) {
-            const uint32_t w0 = ld_shared_u32(stg + t * D + 8 * cc), w1 = ld_shared_u32(stg + t * D + 8 * cc + 4);
-            res[0] = e4m3x2_h2(w0); res[1] = e4m3x2_h2(w0 >> 16); res[2] = e4m3x2_h2(w1); res[3] = e4m3x2_h2(w1 >> 16);
-          } else if constexpr (FMT == KVQ_FMT_HQ2B_TOK) {
-            res[0] = res[1] = res[2] = res[3] = 0u;   // (the split path below writes this format's tile)
+            res[0] = e4m3x2_h2(ra); res[1] = e4m3x2_h2(ra >> 16); res[2] = e4m3x2_h2(rb); res[3] = e4m3x2_h2(rb >> 16);
           } else {
-            dq_pairs(ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc), ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1), res);
+            dq_pairs(ra, rb, res);
 #pragma unroll
             for (int p = 0; p < 4; p++) res[p] = h2u(__hmul2(__hfma2(u2h(res[p]), two, m11), u2h(scs[p])));
           }
@@ -539,8 +548,8 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
         // pair hi = fp16(k^), lo = fp16(k^ - hi), in the two halves of the K buffer
         // (rotated format: the key's rotated coordinates s_d (2c - 3) turned back by H, a warp per
         // key row, lane cc holding dims 8cc .. 8cc + 7)
-        auto key_split = [&](int t, uint4& hi, uint4& lo) {
-          const uint32_t code = ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc) | (ld_shared_u8(stg + t * HQ2B_ROW + 2 * cc + 1) << 8);
+        auto key_split = [&](uint32_t ra, uint32_t rb, uint32_t rm, uint4& hi, uint4& lo) {
+          const uint32_t code = ra | (rb << 8);
           float v[8];
           if constexpr (FMT == KVQ_FMT_HQ2B_HAD) {
 #pragma unroll
@@ -551,8 +560,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
             }
             warp_fwht256(v);
           } else {
-            const uint32_t meta = ld_shared_u32(stg + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
-            const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu)), zf = half_bits_to_float((uint16_t)(meta >> 16));
+            const float sf = half_bits_to_float((uint16_t)(rm & 0xFFFFu)), zf = half_bits_to_float((uint16_t)(rm >> 16));
 #pragma unroll
             for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
           }
@@ -567,17 +575,26 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           hi = make_uint4(h[0], h[1], h[2], h[3]);
           lo = make_uint4(l[0], l[1], l[2], l[3]);
         };
-        if (LY::KSPLIT && key0 + P <= ef) {
-#pragma unroll 4
-          for (int t = t0; t < P; t += KSTEP) {
-            uint4 hi, lo;
-            key_split(t, hi, lo);
-            st_shared_v4(kb + swz(t, cc & 7), hi);
-            st_shared_v4(kb + 32768 + swz(t, cc & 7), lo);
+        if (key0 + P <= ef) {   // every key of the tile comes from the page (ef <= len)
+          // every raw word of the thread's keys first (the loads overlap), then convert and store
+          uint32_t ra[DQ_MAXI], rb[DQ_MAXI], rm[DQ_MAXI];
+#pragma unroll
+          for (int k = 0; k < DQ_MAXI; k++)
+            if (t0 + KSTEP * k < P) key_raw(t0 + KSTEP * k, ra[k], rb[k], rm[k]);
+#pragma unroll
+          for (int k = 0; k < DQ_MAXI; k++) {
+            const int t = t0 + KSTEP * k;
+            if (t < P) {
+              if constexpr (LY::KSPLIT) {
+                uint4 hi, lo;
+                key_split(ra[k], rb[k], rm[k], hi, lo);
+                st_shared_v4(kb + swz(t, cc & 7), hi);
+                st_shared_v4(kb + 32768 + swz(t, cc & 7), lo);
+              } else {
+                st_shared_v4(kb + swz(t, cc & 7), key_code(ra[k], rb[k]));
+              }
+            }
           }
-        } else if (key0 + P <= ef) {   // every key of the tile comes from the page (ef <= len)
-#pragma unroll 4
-          for (int t = t0; t < P; t += KSTEP) st_shared_v4(kb + swz(t, cc & 7), key_code(t));
         } else
 #pragma unroll 4
         for (int t = t0; t < P; t += KSTEP) {
@@ -591,10 +608,11 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
               o.y = h2u(__floats2half2_rn(bf16_lo(w.y), bf16_hi(w.y)));
               o.z = h2u(__floats2half2_rn(bf16_lo(w.z), bf16_hi(w.z)));
               o.w = h2u(__floats2half2_rn(bf16_lo(w.w), bf16_hi(w.w)));
-            } else if constexpr (LY::KSPLIT) {
-              key_split(t, o, olo);
             } else {
-              o = key_code(t);
+              uint32_t ra = 0u, rb = 0u, rm = 0u;
+              key_raw(t, ra, rb, rm);
+              if constexpr (LY::KSPLIT) key_split(ra, rb, rm, o, olo);
+              else o = key_code(ra, rb);
             }
           }
           st_shared_v4(kb + swz(t, cc & 7), o);
@@ -609,38 +627,56 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
       const uint32_t vb = sm_u32(smem + LY::SM_V + buf * LY::V_BUF) + tile_off;
       const uint32_t vst = stg + block_bytes(LY::LFMT);
       const bool vall = key0 + P <= len;
-#pragma unroll 4
-      for (int t = t0; t < P; t += KSTEP) {
-        uint4 o = make_uint4(0u, 0u, 0u, 0u), olo = make_uint4(0u, 0u, 0u, 0u);
-        if (vall || key0 + t < len) {
-          if constexpr (FP8) {
-            const uint32_t w0 = ld_shared_u32(vst + t * D + 8 * cc), w1 = ld_shared_u32(vst + t * D + 8 * cc + 4);
-            o = make_uint4(e4m3x2_h2(w0), e4m3x2_h2(w0 >> 16), e4m3x2_h2(w1), e4m3x2_h2(w1 >> 16));
-          } else if constexpr (FMT == KVQ_FMT_HQ2B_HAD) {
-            // v^ = H (z + c s): the rotated row dequantized in fp32, turned back by the warp
-            const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
-            const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
-            const float zf = half_bits_to_float((uint16_t)(meta >> 16));
-            const uint32_t code =
-                ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc) | (ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1) << 8);
-            float v[8];
+      {
+        // raw words of the thread's value rows first (codes or E4M3 words, and the meta word),
+        // then convert and store; rows past the sequence are stored as zeros
+        uint32_t ra[DQ_MAXI], rb[DQ_MAXI], rm[DQ_MAXI];
 #pragma unroll
-            for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
-            warp_fwht256(v);
-            o = make_uint4(h2u(__floats2half2_rn(v[0], v[1])), h2u(__floats2half2_rn(v[2], v[3])),
-                           h2u(__floats2half2_rn(v[4], v[5])), h2u(__floats2half2_rn(v[6], v[7])));
-          } else {
-            const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
-            const __half2 s2 = u2h(__byte_perm(meta, 0u, 0x1010u)), z2 = u2h(__byte_perm(meta, 0u, 0x3232u));
-            uint32_t res[4];
-            dq_pairs(ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc), ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1), res);
-#pragma unroll
-            for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
-            o = make_uint4(res[0], res[1], res[2], res[3]);
+        for (int k = 0; k < DQ_MAXI; k++) {
+          const int t = t0 + KSTEP * k;
+          if (t < P && (vall || key0 + t < len)) {
+            if constexpr (FP8) {
+              ra[k] = ld_shared_u32(vst + t * D + 8 * cc);
+              rb[k] = ld_shared_u32(vst + t * D + 8 * cc + 4);
+            } else {
+              rm[k] = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+              ra[k] = ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc);
+              rb[k] = ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1);
+            }
           }
         }
-        st_shared_v4(vb + swz(t, cc & 7), o);
-        if constexpr (LY::VSPLIT) st_shared_v4(vb + 32768 + swz(t, cc & 7), olo);
+#pragma unroll
+        for (int k = 0; k < DQ_MAXI; k++) {
+          const int t = t0 + KSTEP * k;
+          if (t >= P) continue;
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          // (the rotated format's warp transform runs on every lane of the warp, valid row or not)
+          if (FMT == KVQ_FMT_HQ2B_HAD || vall || key0 + t < len) {
+            const bool valid = vall || key0 + t < len;
+            if constexpr (FP8) {
+              o = make_uint4(e4m3x2_h2(ra[k]), e4m3x2_h2(ra[k] >> 16), e4m3x2_h2(rb[k]), e4m3x2_h2(rb[k] >> 16));
+            } else if constexpr (FMT == KVQ_FMT_HQ2B_HAD) {
+              // v^ = H (z + c s): the rotated row dequantized in fp32, turned back by the warp
+              const uint32_t meta = valid ? rm[k] : 0u, code = valid ? (ra[k] | (rb[k] << 8)) : 0u;
+              const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
+              const float zf = half_bits_to_float((uint16_t)(meta >> 16));
+              float v[8];
+#pragma unroll
+              for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
+              warp_fwht256(v);
+              o = make_uint4(h2u(__floats2half2_rn(v[0], v[1])), h2u(__floats2half2_rn(v[2], v[3])),
+                             h2u(__floats2half2_rn(v[4], v[5])), h2u(__floats2half2_rn(v[6], v[7])));
+            } else {
+              const __half2 s2 = u2h(__byte_perm(rm[k], 0u, 0x1010u)), z2 = u2h(__byte_perm(rm[k], 0u, 0x3232u));
+              uint32_t res[4];
+              dq_pairs(ra[k], rb[k], res);
+#pragma unroll
+              for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
+              o = make_uint4(res[0], res[1], res[2], res[3]);
+            }
+          }
+          st_shared_v4(vb + swz(t, cc & 7), o);
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       __syncwarp();
@@ -648,7 +684,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
         bar_arrive(BAR(B_V_FULL + buf));
         bar_arrive(BAR(B_STG_EMPTY + sbuf));
       }
-      if (tid == 0 && issued < ntiles) {
+      // the copier refills the stage of tile j - 1 (not of tile j, which the other warps may
+      // still be reading), so its wait rarely holds up its own warp
+      if (tid == 0 && j >= 1 && issued < ntiles) {
         if (!issue(issued)) timed_out = true;
         issued++;
       }
@@ -690,12 +728,6 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
         for (int ks = 0; ks < 4; ks++)
           tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_mn_desc(vb + 2048 * ks), IDESC_PV,
                     (j > 0 || ks > 0) ? 1u : 0u);
-        if constexpr (LY::VSPLIT) {   // + P . V_lo: the low parts of the values
-#pragma unroll
-          for (int ks = 0; ks < 4; ks++)
-            tc_mma_ts(tmem + TM_O, tmem + TM_S0 + 64 * buf + 8 * ks, sw128_mn_desc(vb + 32768 + 2048 * ks), IDESC_PV,
-                      1u);
-        }
         tc_commit(BAR(B_PV_DONE + buf));
       };
       int last_pv = -1;
