@@ -34,6 +34,7 @@ constexpr int PT_DQ_WARPS = 7;                    // TMA + dequantisation warps 
 constexpr int PT_MMA_WARP = 4 + PT_DQ_WARPS;      // the warp whose lane 0 issues the MMAs
 constexpr int PT_THREADS = (PT_MMA_WARP + 1) * 32;
 constexpr int SM_K = 0;                   // 2 K tile buffers
+constexpr int PT_MAX_TILES = PREFILL_SPLIT / P;   // 64-key tiles of one split (a CTA's keys)
 
 // Per page format.  The staging ring holds a page's K and V blocks of one (layer, head) as one
 // bulk copy a stage: 9,216 B for the 2-bit layouts (6 stages), 32 KB for FP8 (2 stages).  Two
@@ -56,7 +57,8 @@ struct PfLayout {
   static constexpr int NUM_BARS = 13 + 2 * NSTG;
   static constexpr int SM_ABORT = SM_BAR + NUM_BARS * 8;
   static constexpr int SM_TMEM = SM_ABORT + 4;
-  static constexpr int SMEM = SM_TMEM + 12 + 1024;   // + slack to align the base to 1,024 B
+  static constexpr int SM_PAGES = SM_TMEM + 16;       // the CTA's page ids, PT_MAX_TILES int32
+  static constexpr int SMEM = SM_PAGES + 4 * PT_MAX_TILES + 1024;   // + slack to align the base to 1,024 B
 };
 constexpr int TM_Q = 0, TM_S0 = 128, TM_O = 256;
 constexpr int PT_SPIN = 1 << 16;
@@ -465,10 +467,13 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
     const int tid = threadIdx.x - 128;             // 0 .. 32 * PT_DQ_WARPS - 1
     constexpr int DQ_T = 32 * PT_DQ_WARPS;
     const int64_t lane_row = (int64_t)b * c.max_pages;
+    // the page ids of the CTA's tiles, read once into shared memory by the copier's warp (the
+    // copies then wait on no global load)
+    int32_t* s_pages = reinterpret_cast<int32_t*>(smem + LY::SM_PAGES);
     auto issue = [&](int j) -> bool {
       const int buf = j % PT_NSTG;
       if (!bar_wait(BAR(B_STG_EMPTY + buf), ((j / PT_NSTG) & 1) ^ 1)) return false;
-      const int32_t phys = c.page_table[lane_row + p0 + j];
+      const int32_t phys = s_pages[j];
       if (phys < 0 || phys >= c.pool_pages) {
         flag(c.status, KVQ_STATUS_PAGE_OOB);
         bar_arrive(BAR(B_STG_FULL + buf));
@@ -486,6 +491,10 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           : "memory");
       return true;
     };
+    if (tid < 32) {
+      for (int jj = tid; jj < ntiles; jj += 32) s_pages[jj] = c.page_table[lane_row + p0 + jj];
+      __syncwarp();
+    }
     int issued = 0;
     if (tid == 0) {
       for (; issued < PT_NSTG && issued < ntiles; issued++)
@@ -775,6 +784,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
 
 template <int FMT>
 static int launch_prefill_fmt(const AttnArgs& a, cudaStream_t stream) {
+  if (a.split_tokens > PREFILL_SPLIT || a.split_tokens % P) return KVQ_ERR_UNSUPPORTED;   // s_pages holds one split
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
