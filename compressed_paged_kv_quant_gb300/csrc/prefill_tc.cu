@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
     const int cc = tid & 31, t0 = tid >> 5;
     constexpr int KSTEP = DQ_T / 32;
     constexpr int DQ_MAXI = (P + KSTEP - 1) / KSTEP;   // keys a thread takes of a tile, at most
+    constexpr bool DQ_BATCH = FMT != KVQ_FMT_HQ2B_HAD;     // all of a tile's loads first
     const uint32_t tile_off = (uint32_t)(cc >> 3) * 8192u;
     for (int j = 0; j < ntiles && !timed_out; j++) {
       const int buf = j & 1;
@@ -584,7 +585,19 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           hi = make_uint4(h[0], h[1], h[2], h[3]);
           lo = make_uint4(l[0], l[1], l[2], l[3]);
         };
-        if (key0 + P <= ef) {   // every key of the tile comes from the page (ef <= len)
+        if (!DQ_BATCH && key0 + P <= ef) {
+          // rotated format: a key row at a time (each row's transform is a long run of shuffles;
+          // a loop unrolled over all of a thread's rows is too much code)
+#pragma unroll 2
+          for (int t = t0; t < P; t += KSTEP) {
+            uint32_t ra = 0u, rb = 0u, rm = 0u;
+            key_raw(t, ra, rb, rm);
+            uint4 hi, lo;
+            key_split(ra, rb, rm, hi, lo);
+            st_shared_v4(kb + swz(t, cc & 7), hi);
+            st_shared_v4(kb + 32768 + swz(t, cc & 7), lo);
+          }
+        } else if (key0 + P <= ef) {   // every key of the tile comes from the page (ef <= len)
           // every raw word of the thread's keys first (the loads overlap), then convert and store
           uint32_t ra[DQ_MAXI], rb[DQ_MAXI], rm[DQ_MAXI];
 #pragma unroll
@@ -636,7 +649,28 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
       const uint32_t vb = sm_u32(smem + LY::SM_V + buf * LY::V_BUF) + tile_off;
       const uint32_t vst = stg + block_bytes(LY::LFMT);
       const bool vall = key0 + P <= len;
-      {
+      if constexpr (!DQ_BATCH) {
+        // rotated format: v^ = H (z + c s), a row at a time (the transform is a long run of
+        // shuffles): the rotated row dequantized in fp32, turned back by the warp
+#pragma unroll 2
+        for (int t = t0; t < P; t += KSTEP) {
+          uint4 o = make_uint4(0u, 0u, 0u, 0u);
+          if (vall || key0 + t < len) {   // (the same for the whole warp: one row a warp)
+            const uint32_t meta = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+            const uint32_t code =
+                ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc) | (ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1) << 8);
+            const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
+            const float zf = half_bits_to_float((uint16_t)(meta >> 16));
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
+            warp_fwht256(v);
+            o = make_uint4(h2u(__floats2half2_rn(v[0], v[1])), h2u(__floats2half2_rn(v[2], v[3])),
+                           h2u(__floats2half2_rn(v[4], v[5])), h2u(__floats2half2_rn(v[6], v[7])));
+          }
+          st_shared_v4(vb + swz(t, cc & 7), o);
+        }
+      } else {
         // raw words of the thread's value rows first (codes or E4M3 words, and the meta word),
         // then convert and store; rows past the sequence are stored as zeros
         uint32_t ra[DQ_MAXI], rb[DQ_MAXI], rm[DQ_MAXI];
@@ -659,22 +693,9 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
           const int t = t0 + KSTEP * k;
           if (t >= P) continue;
           uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          // (the rotated format's warp transform runs on every lane of the warp, valid row or not)
-          if (FMT == KVQ_FMT_HQ2B_HAD || vall || key0 + t < len) {
-            const bool valid = vall || key0 + t < len;
+          if (vall || key0 + t < len) {
             if constexpr (FP8) {
               o = make_uint4(e4m3x2_h2(ra[k]), e4m3x2_h2(ra[k] >> 16), e4m3x2_h2(rb[k]), e4m3x2_h2(rb[k] >> 16));
-            } else if constexpr (FMT == KVQ_FMT_HQ2B_HAD) {
-              // v^ = H (z + c s): the rotated row dequantized in fp32, turned back by the warp
-              const uint32_t meta = valid ? rm[k] : 0u, code = valid ? (ra[k] | (rb[k] << 8)) : 0u;
-              const float sf = half_bits_to_float((uint16_t)(meta & 0xFFFFu));
-              const float zf = half_bits_to_float((uint16_t)(meta >> 16));
-              float v[8];
-#pragma unroll
-              for (int e = 0; e < 8; e++) v[e] = fmaf((float)((code >> (2 * e)) & 3u), sf, zf);
-              warp_fwht256(v);
-              o = make_uint4(h2u(__floats2half2_rn(v[0], v[1])), h2u(__floats2half2_rn(v[2], v[3])),
-                             h2u(__floats2half2_rn(v[4], v[5])), h2u(__floats2half2_rn(v[6], v[7])));
             } else {
               const __half2 s2 = u2h(__byte_perm(rm[k], 0u, 0x1010u)), z2 = u2h(__byte_perm(rm[k], 0u, 0x3232u));
               uint32_t res[4];
