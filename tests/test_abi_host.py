@@ -207,3 +207,33 @@ def test_noalloc_host_validation_matches_decode(L):
     huge = 1 << 22
     assert kvq.decode_workspace_bytes(g, 4096, huge) > kvq.NOALLOC_SCRATCH_BYTES
     assert _noalloc(L, g, lanes=4096, max_seq_len=huge, max_pages=huge // 64) == kvq.ERR_SCRATCH_LIMIT
+
+
+def test_selftest_wait_timeout_host_validation(L):
+    """The bounded-wait self-test refuses a null status word on the host, before any launch."""
+    assert L.kvq_selftest_wait_timeout(None, None) == kvq.ERR_INVALID_ARG
+
+
+def _step(L, g, **kw):
+    a = dict(layer=0, pool=256, pool_bytes=1 << 24, ring=512, window=0, pt=768, max_pages=4, lanes=1,
+             start=2304, n_new=2560, tok_off=2816, n_rows=1, k=3072, v=3328, seq_len=1024, max_seq_len=256,
+             q=1280, scale=0.0625, ws=1536, ws_bytes=1 << 24, out=1792, status=2048)
+    a.update(kw)
+    return L.kvq_decode_step(ctypes.byref(g), a["layer"], a["pool"], a["pool_bytes"], a["ring"], a["window"],
+                             a["pt"], a["max_pages"], a["lanes"], a["start"], a["n_new"], a["tok_off"], a["n_rows"],
+                             a["k"], a["v"], a["seq_len"], a["max_seq_len"], a["q"], a["scale"], a["ws"],
+                             a["ws_bytes"], a["out"], a["status"], None)
+
+
+@pytest.mark.parametrize("window", [0, 64])
+def test_decode_step_host_validation(L, window):
+    """kvq_decode_step checks the append's arguments and the attention's before it launches
+    anything, in both launch orders (window 64: the append runs last)."""
+    g = kvq.geom(kvq.FMT_HQ2B, 2, 1, 4)
+    assert _step(L, g, window=window, start=None) == kvq.ERR_INVALID_ARG
+    assert _step(L, g, window=window, n_rows=-1) == kvq.ERR_INVALID_ARG
+    assert _step(L, g, window=window, k=3080) == kvq.ERR_ALIGNMENT
+    assert _step(L, g, window=window, v=None) == kvq.ERR_INVALID_ARG
+    assert _step(L, g, window=window, ws_bytes=64) == kvq.ERR_WORKSPACE_TOO_SMALL
+    assert _step(L, g, window=window, layer=2) == kvq.ERR_INVALID_ARG
+    assert _step(L, g, window=window, lanes=0) == kvq.OK
