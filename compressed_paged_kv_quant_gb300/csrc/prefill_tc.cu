@@ -672,40 +672,49 @@ __global__ void __launch_bounds__(PT_THREADS, 1) prefill_tc(AttnArgs a) {
         }
       } else {
         // raw words of the thread's value rows first (codes or E4M3 words, and the meta word),
-        // then convert and store; rows past the sequence are stored as zeros
+        // then convert and store; rows past the sequence are stored as zeros (only the last
+        // tile has such rows: the others take a path without a per-row test)
         uint32_t ra[DQ_MAXI], rb[DQ_MAXI], rm[DQ_MAXI];
-#pragma unroll
-        for (int k = 0; k < DQ_MAXI; k++) {
-          const int t = t0 + KSTEP * k;
-          if (t < P && (vall || key0 + t < len)) {
-            if constexpr (FP8) {
-              ra[k] = ld_shared_u32(vst + t * D + 8 * cc);
-              rb[k] = ld_shared_u32(vst + t * D + 8 * cc + 4);
-            } else {
-              rm[k] = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
-              ra[k] = ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc);
-              rb[k] = ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1);
-            }
+        auto v_load = [&](int k, int t) {
+          if constexpr (FP8) {
+            ra[k] = ld_shared_u32(vst + t * D + 8 * cc);
+            rb[k] = ld_shared_u32(vst + t * D + 8 * cc + 4);
+          } else {
+            rm[k] = ld_shared_u32(vst + HQ2B_META_OFF + t * 8 + 4 * (cc >> 4));
+            ra[k] = ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc);
+            rb[k] = ld_shared_u8(vst + t * HQ2B_ROW + 2 * cc + 1);
           }
-        }
+        };
+        auto v_conv = [&](int k) -> uint4 {
+          if constexpr (FP8) {
+            return make_uint4(e4m3x2_h2(ra[k]), e4m3x2_h2(ra[k] >> 16), e4m3x2_h2(rb[k]), e4m3x2_h2(rb[k] >> 16));
+          } else {
+            const __half2 s2 = u2h(__byte_perm(rm[k], 0u, 0x1010u)), z2 = u2h(__byte_perm(rm[k], 0u, 0x3232u));
+            uint32_t res[4];
+            dq_pairs(ra[k], rb[k], res);
 #pragma unroll
-        for (int k = 0; k < DQ_MAXI; k++) {
-          const int t = t0 + KSTEP * k;
-          if (t >= P) continue;
-          uint4 o = make_uint4(0u, 0u, 0u, 0u);
-          if (vall || key0 + t < len) {
-            if constexpr (FP8) {
-              o = make_uint4(e4m3x2_h2(ra[k]), e4m3x2_h2(ra[k] >> 16), e4m3x2_h2(rb[k]), e4m3x2_h2(rb[k] >> 16));
-            } else {
-              const __half2 s2 = u2h(__byte_perm(rm[k], 0u, 0x1010u)), z2 = u2h(__byte_perm(rm[k], 0u, 0x3232u));
-              uint32_t res[4];
-              dq_pairs(ra[k], rb[k], res);
-#pragma unroll
-              for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
-              o = make_uint4(res[0], res[1], res[2], res[3]);
-            }
+            for (int p = 0; p < 4; p++) res[p] = h2u(__hfma2(__hfma2(u2h(res[p]), one2, m4), s2, z2));
+            return make_uint4(res[0], res[1], res[2], res[3]);
           }
-          st_shared_v4(vb + swz(t, cc & 7), o);
+        };
+        if (vall) {
+#pragma unroll
+          for (int k = 0; k < DQ_MAXI; k++)
+            if (t0 + KSTEP * k < P) v_load(k, t0 + KSTEP * k);
+#pragma unroll
+          for (int k = 0; k < DQ_MAXI; k++)
+            if (t0 + KSTEP * k < P) st_shared_v4(vb + swz(t0 + KSTEP * k, cc & 7), v_conv(k));
+        } else {
+#pragma unroll
+          for (int k = 0; k < DQ_MAXI; k++) {
+            const int t = t0 + KSTEP * k;
+            if (t < P && key0 + t < len) v_load(k, t);
+          }
+#pragma unroll
+          for (int k = 0; k < DQ_MAXI; k++) {
+            const int t = t0 + KSTEP * k;
+            if (t < P) st_shared_v4(vb + swz(t, cc & 7), key0 + t < len ? v_conv(k) : make_uint4(0u, 0u, 0u, 0u));
+          }
         }
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
